@@ -1,0 +1,187 @@
+/*
+ * smd.h -- C ABI of libsmd: sparse MLA decode over an fp8_ds_mla paged latent cache,
+ * hand-written CUDA for NVIDIA GB300 (sm_103a).
+ *
+ * One decode step, per query token t (one token per request), computes
+ *
+ *   1. index conversion: the token's request-local top-k indices and sliding-window
+ *      indices become global cache slots through the block table
+ *      (vLLM PR #41217 report, "关键源码片段", _convert_req_index_to_global_index_kernel;
+ *      page-range guard as in vLLM PR #52212 report, "关键源码片段", cp-gather kernel);
+ *   2. row gather + dequantisation of every valid slot into a 512-wide bf16 latent that
+ *      serves as both K and V (SGLang PR #26208 report, "关键源码片段",
+ *      _gather_dequant_dsv4_kernel and the DSV4 row constants);
+ *   3. partial attention: one 512-wide QK dot for all heads, masking of invalid
+ *      entries, softmax, PV over the same 512 dims (vLLM PR #52212 report, "实现拆解"
+ *      item 1: 512-wide QK dot, 4 x 128 PV accumulators, masked tail, attention sink,
+ *      invalid-index semantics);
+ *   4. a workload-aware split-K selector, 1..32 splits (same report, "实现拆解" item 2);
+ *   5. a log-sum-exp combine of split partials that also adds the per-head sink logit
+ *      to the softmax denominator (same report, test symbol _launch_sparse_decode_reduce).
+ *
+ * Cache format.  A page of P = block_size slots is P * 584 bytes: first the P data rows
+ * of 576 bytes (448 fp8 e4m3 NoPE values, then 64 little-endian bf16 RoPE values), then
+ * the P scale rows of 8 bytes (7 UE8M0 codes, one per 64 NoPE values, then one pad
+ * byte).  Global slot g lives in page g / P at offset g % P.  Latent element d < 448 is
+ * e4m3(byte d) * 2^(code[d/64] - 127); element 448 + r is RoPE value r.  An element
+ * that is not finite once held as bf16 (NaN byte, code 255, non-finite RoPE, overflow)
+ * is replaced by 0: the cache is never trusted to be NaN-free (vLLM PR #52212 report,
+ * "实现拆解" item 3).
+ *
+ * Semantics (float64 definition, up to bf16/fp32 rounding):
+ *   s[h,e]  = scale * q[t,h,:] . k_e              over the valid entries e of token t
+ *   den[h]  = sum_e exp(s[h,e]) + exp(sink[h])      (sink term absent if sink == NULL)
+ *   out[t,h,:] = sum_e exp(s[h,e]) k_e / den[h]     (0 when den has no terms)
+ *   lse[t,h]   = ln den[h]                           (-inf when den has no terms)
+ * Entries count once per occurrence (no de-duplication across or within scopes).
+ *
+ * Conventions for every call:
+ *   - All pointers except the dims structs and host outputs are DEVICE pointers of the
+ *     current CUDA device; the caller owns every buffer.  Only smd_read_status
+ *     synchronises; every other call is asynchronous on `stream` (NULL = legacy stream).
+ *   - q, out, kv_cache, kv_out, o_part and workspace must be 16-byte aligned.
+ *   - Bad argument VALUES of the inputs (indices -1 or out of range, block-table entries
+ *     -1 or out of range, request ids out of range) are masked, never errors.
+ *   - Errors: SMD_ERR_INVALID_ARG for bad shapes/pointers (nothing is launched),
+ *     SMD_ERR_WORKSPACE for a too-small workspace, SMD_ERR_UNSUPPORTED for a shape the
+ *     kernels do not cover, SMD_ERR_CUDA when a launch fails.  smd_last_error() then
+ *     returns a message (thread-local, valid until the next call on this thread).
+ */
+#ifndef SMD_H_
+#define SMD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMD_API __attribute__((visibility("default")))
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *smd_stream_t;
+
+enum {
+  SMD_OK = 0,
+  SMD_ERR_INVALID_ARG = -1,
+  SMD_ERR_UNSUPPORTED = -2,
+  SMD_ERR_WORKSPACE = -3,
+  SMD_ERR_CUDA = -4,
+  SMD_ERR_TIMEOUT = -5
+};
+
+#define SMD_LATENT_DIM 512
+#define SMD_ROW_BYTES 584
+#define SMD_MAX_HEADS 128
+#define SMD_MAX_SPLITS 32
+
+/* Shapes shared by the calls.  Counts are elements; strides are elements between rows. */
+typedef struct smd_dims {
+  int32_t num_tokens;          /* T in [0, 65535]: query tokens (one per request)       */
+  int32_t num_heads;           /* H in [1, 128]: query heads; one shared latent KV head  */
+  int32_t num_requests;        /* R >= 1: rows of block_table                           */
+  int32_t max_blocks_per_req;  /* >= 1: valid columns of block_table                    */
+  int64_t num_pages;           /* >= 1: pages in kv_cache; num_pages*block_size < 2^31   */
+  int32_t block_size;          /* P >= 1: slots per page (64 for the DSV4 cache)         */
+  int32_t topk;                /* K >= 0: top-k entries per token                       */
+  int32_t swa;                 /* W >= 0: sliding-window entries per token              */
+  int32_t pad_;                /* reserved, set to 0                                    */
+  int64_t bt_stride;           /* >= max_blocks_per_req: block_table row stride         */
+  int64_t topk_stride;         /* >= topk: topk_idx row stride                          */
+  int64_t swa_stride;          /* >= swa: swa_idx row stride                            */
+} smd_dims;
+
+/*
+ * Split selector (host only, no device call unless num_sms <= 0).  Returns the number of
+ * split-K parts S the decode will use, or a negative status.  num_splits: 0 = automatic
+ * with cap 32; n > 0 = automatic with cap n; n < 0 = exactly -n (1..32).  The automatic
+ * choice depends only on the shapes and num_sms, so a captured CUDA graph stays valid:
+ * "short" steps (K+W <= 1024 entries) cap at 4 splits; otherwise the count that
+ * minimises (CTA waves x tiles per split) over 1..cap, each split keeping >= 1 tile
+ * (vLLM PR #52212 report, "实现拆解" item 2: occupancy target, short work <= 4, low-batch
+ * long context up to 32).  num_sms <= 0 means "the current device's SM count".
+ */
+SMD_API int smd_select_num_splits(const smd_dims *dims, int num_splits, int num_sms);
+
+/*
+ * Device workspace bytes smd_sparse_mla_decode needs for the given split request
+ * (same num_splits/num_sms meaning as smd_select_num_splits).  Holds a status word,
+ * the converted indices [T, K+W] int32 and, when S > 1, the split partials
+ * o_part f32 [T, S, H, 512] and lse_part f32 [T, S, H].  Returns 0 on bad dims.
+ */
+SMD_API size_t smd_workspace_size(const smd_dims *dims, int num_splits, int num_sms);
+
+/*
+ * The whole decode step (conversion, fused gather + dequant + tcgen05 attention, and
+ * the LSE combine when S > 1).
+ *   q           bf16 [T, H, 512], row-major, the latent order [NoPE 448 | RoPE 64]
+ *   kv_cache    u8   [num_pages, block_size * 584] (format above)
+ *   block_table i32  [R, bt_stride]: page of block b of request r, -1 = unused
+ *   req_id      i32  [T]: request of token t
+ *   topk_idx    i32  [T, topk_stride] request-local positions, -1 = none (NULL iff K=0)
+ *   swa_idx     i32  [T, swa_stride]  request-local positions, -1 = none (NULL iff W=0)
+ *   sink        f32  [H] per-head sink logits in the scaled-score domain, or NULL
+ *   scale       softmax scale applied to q . k (e.g. 1/sqrt(512))
+ *   out         bf16 [T, H, 512] (written)
+ *   lse         f32  [T, H] natural-log denominator including the sink, or NULL
+ *   num_splits  split request, as for smd_select_num_splits
+ *   workspace   >= smd_workspace_size(dims, num_splits, device SMs) bytes, 16-B aligned;
+ *               its first 4 bytes are a device status word (0 = ok) that the call
+ *               resets and that a kernel sets if one of its bounded waits gives up
+ */
+SMD_API int smd_sparse_mla_decode(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
+                                  const int32_t *block_table, const int32_t *req_id,
+                                  const int32_t *topk_idx, const int32_t *swa_idx,
+                                  const float *sink, float scale, void *out, float *lse,
+                                  int num_splits, void *workspace, size_t workspace_bytes,
+                                  smd_stream_t stream);
+
+/*
+ * Step 1 alone: writes gidx i32 [T, K+W] (top-k entries first, window entries at
+ * offset K) with the global slot of each valid entry and -1 for every invalid one
+ * (index < 0, block outside [0, max_blocks), page outside [0, num_pages), request id
+ * outside [0, R)).
+ */
+SMD_API int smd_convert_req_index(const smd_dims *dims, const int32_t *block_table,
+                                  const int32_t *req_id, const int32_t *topk_idx,
+                                  const int32_t *swa_idx, int32_t *gidx, smd_stream_t stream);
+
+/*
+ * Step 2 alone (a test and debugging export): for each of num_rows global slots
+ * gidx[i] writes the dequantised bf16 latent row kv_out[i, 0:512]; a slot that is
+ * negative or >= num_pages * block_size gives a zero row.  Only dims->num_pages and
+ * dims->block_size are read.
+ */
+SMD_API int smd_gather_dequant(const smd_dims *dims, const uint8_t *kv_cache, const int32_t *gidx,
+                               int64_t num_rows, void *kv_out, smd_stream_t stream);
+
+/*
+ * Step 5 alone: merges S split partials per (token, head).  o_part f32 [T, S, H, 512]
+ * holds each split's output normalised over its own entries, lse_part f32 [T, S, H]
+ * its natural-log denominator without sink (-inf for an empty split).  Writes
+ * out bf16 [T, H, 512] and, if non-NULL, lse f32 [T, H]; sink may be NULL.
+ * Requires 1 <= S <= 32 and 1 <= H.
+ */
+SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_heads,
+                            const float *o_part, const float *lse_part, const float *sink,
+                            void *out, float *lse, smd_stream_t stream);
+
+/*
+ * Reads the device status word at the start of a decode workspace into *device_status
+ * after synchronising `stream`.  Returns SMD_ERR_TIMEOUT if a kernel recorded that a
+ * bounded wait gave up, SMD_OK otherwise (or SMD_ERR_CUDA if the copy fails).
+ */
+SMD_API int smd_read_status(const void *workspace, int32_t *device_status, smd_stream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+SMD_API const char *smd_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+SMD_API int smd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMD_H_ */

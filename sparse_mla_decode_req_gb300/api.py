@@ -1,0 +1,215 @@
+"""Thin ctypes binding of libsmd (``include/smd.h``), with the same names.
+
+Argument marshalling only: shapes, strides and device pointers are read from torch
+tensors and passed to the C ABI; every step of the decode runs in the library's CUDA
+kernels.  There is no CPU fallback: if ``libsmd.so`` is missing or fails to load, the
+first call raises.  Build it with ``python -m sparse_mla_decode_req_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsmd.so")
+
+SMD_OK = 0
+SMD_ERR_INVALID_ARG = -1
+SMD_ERR_UNSUPPORTED = -2
+SMD_ERR_WORKSPACE = -3
+SMD_ERR_CUDA = -4
+SMD_ERR_TIMEOUT = -5
+LATENT_DIM = 512
+ROW_BYTES = 584
+MAX_SPLITS = 32
+
+
+class SmdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libsmd status {status}: {message}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    """``smd_dims`` (include/smd.h)."""
+
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("num_requests", ctypes.c_int32),
+        ("max_blocks_per_req", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64),
+        ("block_size", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("swa", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+        ("bt_stride", ctypes.c_int64),
+        ("topk_stride", ctypes.c_int64),
+        ("swa_stride", ctypes.c_int64),
+    ]
+
+
+_lib = None
+
+# name -> (restype, argtypes), mirroring include/smd.h
+_P = ctypes.c_void_p
+_SIGS = {
+    "smd_select_num_splits": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int]),
+    "smd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int]),
+    "smd_sparse_mla_decode": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
+                                             _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "smd_convert_req_index": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P]),
+    "smd_gather_dequant": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, ctypes.c_int64, _P, _P]),
+    "smd_lse_combine": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P]),
+    "smd_read_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "smd_last_error": (ctypes.c_char_p, []),
+    "smd_version": (ctypes.c_int, []),
+}
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libsmd.so once; raise if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"{_LIB_PATH} is not built; run python -m sparse_mla_decode_req_gb300.build")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def last_error() -> str:
+    return load().smd_last_error().decode()
+
+
+def _check(status: int) -> int:
+    if status < 0:
+        raise SmdError(status, last_error())
+    return status
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _row_stride(t, n_cols):
+    if t is None or n_cols == 0:
+        return max(n_cols, 0)
+    assert t.dtype == torch.int32 and t.dim() == 2 and t.stride(1) == 1, \
+        "index tensors: int32 [rows, cols], unit column stride"
+    return t.stride(0)
+
+
+def make_dims(q, kv_cache, block_table, req_id, topk_idx, swa_idx, block_size: int = 64) -> Dims:
+    """smd_dims from tensor shapes (q [T,H,512], kv_cache [pages, P*584], block_table [R, B])."""
+    T = int(req_id.shape[0])
+    H = int(q.shape[1]) if q is not None else 1
+    K = 0 if topk_idx is None else int(topk_idx.shape[1])
+    W = 0 if swa_idx is None else int(swa_idx.shape[1])
+    return Dims(num_tokens=T, num_heads=H, num_requests=int(block_table.shape[0]),
+                max_blocks_per_req=int(block_table.shape[1]), num_pages=int(kv_cache.shape[0]),
+                block_size=int(block_size), topk=K, swa=W, pad_=0,
+                bt_stride=_row_stride(block_table, int(block_table.shape[1])),
+                topk_stride=_row_stride(topk_idx, K), swa_stride=_row_stride(swa_idx, W))
+
+
+def select_num_splits(dims: Dims, num_splits: int = 0, num_sms: int = 0) -> int:
+    return _check(load().smd_select_num_splits(ctypes.byref(dims), int(num_splits), int(num_sms)))
+
+
+def workspace_size(dims: Dims, num_splits: int = 0, num_sms: int = 0) -> int:
+    n = load().smd_workspace_size(ctypes.byref(dims), int(num_splits), int(num_sms))
+    if n == 0:
+        raise SmdError(SMD_ERR_INVALID_ARG, last_error())
+    return int(n)
+
+
+def sparse_mla_decode(q, kv_cache, block_table, req_id, topk_idx, swa_idx, sink, scale: float,
+                      out=None, lse=None, num_splits: int = 0, workspace=None, block_size: int = 64,
+                      stream=None, return_lse: bool = True):
+    """Run one decode step; returns (out bf16 [T,H,512], lse f32 [T,H] or None)."""
+    dims = make_dims(q, kv_cache, block_table, req_id, topk_idx, swa_idx, block_size)
+    T, H = dims.num_tokens, dims.num_heads
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, LATENT_DIM, dtype=torch.bfloat16, device=dev)
+    if lse is None and return_lse:
+        lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = workspace_size(dims, num_splits, torch.cuda.get_device_properties(dev).multi_processor_count)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    for name, t in (("q", q), ("kv_cache", kv_cache), ("out", out)):
+        assert t.is_contiguous(), f"{name} must be contiguous"
+    _check(load().smd_sparse_mla_decode(
+        ctypes.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(req_id), _ptr(topk_idx),
+        _ptr(swa_idx), _ptr(sink), ctypes.c_float(scale), _ptr(out), _ptr(lse), int(num_splits),
+        _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream)))
+    return out, lse
+
+
+def convert_req_index(block_table, req_id, topk_idx, swa_idx, num_pages: int, block_size: int = 64,
+                      gidx=None, stream=None):
+    """Request-local indices -> global slots, int32 [T, K+W] (-1 = invalid)."""
+    T = int(req_id.shape[0])
+    K = 0 if topk_idx is None else int(topk_idx.shape[1])
+    W = 0 if swa_idx is None else int(swa_idx.shape[1])
+    dims = Dims(num_tokens=T, num_heads=1, num_requests=int(block_table.shape[0]),
+                max_blocks_per_req=int(block_table.shape[1]), num_pages=int(num_pages),
+                block_size=int(block_size), topk=K, swa=W, pad_=0,
+                bt_stride=_row_stride(block_table, int(block_table.shape[1])),
+                topk_stride=_row_stride(topk_idx, K), swa_stride=_row_stride(swa_idx, W))
+    if gidx is None:
+        gidx = torch.empty(T, K + W, dtype=torch.int32, device=block_table.device)
+    _check(load().smd_convert_req_index(ctypes.byref(dims), _ptr(block_table), _ptr(req_id), _ptr(topk_idx),
+                                        _ptr(swa_idx), _ptr(gidx), _stream(stream)))
+    return gidx
+
+
+def gather_dequant(kv_cache, gidx, block_size: int = 64, kv_out=None, stream=None):
+    """Dequantised bf16 latent rows [n, 512] for the global slots in gidx (zero rows if invalid)."""
+    flat = gidx.reshape(-1)
+    assert flat.dtype == torch.int32 and flat.is_contiguous()
+    n = flat.numel()
+    if kv_out is None:
+        kv_out = torch.empty(n, LATENT_DIM, dtype=torch.bfloat16, device=kv_cache.device)
+    dims = Dims(num_tokens=0, num_heads=1, num_requests=1, max_blocks_per_req=1,
+                num_pages=int(kv_cache.shape[0]), block_size=int(block_size))
+    _check(load().smd_gather_dequant(ctypes.byref(dims), _ptr(kv_cache), _ptr(flat), ctypes.c_int64(n),
+                                     _ptr(kv_out), _stream(stream)))
+    return kv_out
+
+
+def lse_combine(o_part, lse_part, sink=None, out=None, lse=None, stream=None):
+    """Merge split partials o_part f32 [T,S,H,512], lse_part f32 [T,S,H] -> (out bf16, lse f32)."""
+    T, S, H, D = o_part.shape
+    assert D == LATENT_DIM and o_part.is_contiguous() and lse_part.is_contiguous()
+    if out is None:
+        out = torch.empty(T, H, D, dtype=torch.bfloat16, device=o_part.device)
+    if lse is None:
+        lse = torch.empty(T, H, dtype=torch.float32, device=o_part.device)
+    _check(load().smd_lse_combine(T, S, H, _ptr(o_part), _ptr(lse_part), _ptr(sink), _ptr(out), _ptr(lse),
+                                  _stream(stream)))
+    return out, lse
+
+
+def read_status(workspace, stream=None) -> int:
+    """Device status word of a decode workspace (0 = ok); raises SmdError on a recorded timeout."""
+    v = ctypes.c_int32(0)
+    _check(load().smd_read_status(_ptr(workspace), ctypes.byref(v), _stream(stream)))
+    return v.value

@@ -1,0 +1,298 @@
+// C-ABI entry points of libsmd (declared in include/smd.h): argument validation, the
+// workload-aware split selector, workspace layout and kernel launches.  Host code only.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "smd.h"
+#include "smd_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SMD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxEntries = 1 << 20;   // K + W per token
+constexpr int32_t kMaxTokens = 65535;      // grid.y limit of the per-token launches
+// Split-selector cost model, in units of one 64-row tile of one CTA: fixed per-CTA work
+// (TMEM allocation, Q staging, epilogue) and the extra combine launch.
+constexpr int kCtaOverheadTiles = 2;
+constexpr int kCombineTiles = 1;
+constexpr int kShortEntries = 1024;
+constexpr int kShortCap = 4;
+
+int check_dims(const smd_dims* d) {
+  if (d == nullptr) return fail(SMD_ERR_INVALID_ARG, "dims is NULL");
+  if (d->num_tokens < 0 || d->num_tokens > kMaxTokens)
+    return fail(SMD_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", d->num_tokens, kMaxTokens);
+  if (d->num_heads < 1 || d->num_heads > SMD_MAX_HEADS)
+    return fail(SMD_ERR_INVALID_ARG, "num_heads %d outside [1, %d]", d->num_heads, SMD_MAX_HEADS);
+  if (d->num_requests < 1) return fail(SMD_ERR_INVALID_ARG, "num_requests %d < 1", d->num_requests);
+  if (d->max_blocks_per_req < 1)
+    return fail(SMD_ERR_INVALID_ARG, "max_blocks_per_req %d < 1", d->max_blocks_per_req);
+  if (d->block_size < 1) return fail(SMD_ERR_INVALID_ARG, "block_size %d < 1", d->block_size);
+  if (d->num_pages < 1) return fail(SMD_ERR_INVALID_ARG, "num_pages %lld < 1", (long long)d->num_pages);
+  if (d->num_pages > (int64_t)INT32_MAX / d->block_size)
+    return fail(SMD_ERR_INVALID_ARG, "num_pages * block_size must stay below 2^31");
+  if (d->topk < 0 || d->swa < 0) return fail(SMD_ERR_INVALID_ARG, "topk/swa must be >= 0");
+  if ((int64_t)d->topk + d->swa > kMaxEntries)
+    return fail(SMD_ERR_INVALID_ARG, "topk + swa = %lld exceeds %lld", (long long)d->topk + d->swa,
+                (long long)kMaxEntries);
+  if (d->bt_stride < d->max_blocks_per_req)
+    return fail(SMD_ERR_INVALID_ARG, "bt_stride %lld < max_blocks_per_req", (long long)d->bt_stride);
+  if (d->topk > 0 && d->topk_stride < d->topk)
+    return fail(SMD_ERR_INVALID_ARG, "topk_stride %lld < topk", (long long)d->topk_stride);
+  if (d->swa > 0 && d->swa_stride < d->swa)
+    return fail(SMD_ERR_INVALID_ARG, "swa_stride %lld < swa", (long long)d->swa_stride);
+  return SMD_OK;
+}
+
+int device_sms(int num_sms) {
+  if (num_sms > 0) return num_sms;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
+int select_splits(const smd_dims* d, int request, int sms) {
+  const int64_t N = (int64_t)d->topk + d->swa;
+  const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
+  if (request < 0) {
+    const int s = -request;
+    return s > smd::kMaxSplits ? smd::kMaxSplits : s;
+  }
+  int cap = request == 0 ? smd::kMaxSplits : (request > smd::kMaxSplits ? smd::kMaxSplits : request);
+  if (N <= kShortEntries && cap > kShortCap) cap = kShortCap;
+  if (tiles < cap) cap = (int)(tiles > 0 ? tiles : 1);
+  if (d->num_tokens == 0 || tiles == 0) return 1;
+  const int64_t cps = smd::attn_ctas_per_split();
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int s = 1; s <= cap; ++s) {
+    const int64_t tps = (tiles + s - 1) / s;
+    if ((int64_t)(s - 1) * tps >= tiles) continue;  // would leave a split without a tile
+    const int64_t ctas = (int64_t)d->num_tokens * s * cps;
+    const int64_t waves = (ctas + sms - 1) / sms;
+    const int64_t cost = waves * (tps + kCtaOverheadTiles) + (s > 1 ? kCombineTiles : 0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+struct Layout {
+  size_t status = 0, gidx = 0, o_part = 0, lse_part = 0, total = 0;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout workspace_layout(const smd_dims* d, int S) {
+  Layout L;
+  const size_t T = (size_t)d->num_tokens, N = (size_t)d->topk + (size_t)d->swa, H = (size_t)d->num_heads;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.gidx = off;
+  off += up256(T * N * sizeof(int32_t));
+  if (S > 1) {
+    L.o_part = off;
+    off += up256(T * (size_t)S * H * SMD_LATENT_DIM * sizeof(float));
+    L.lse_part = off;
+    off += up256(T * (size_t)S * H * sizeof(float));
+  }
+  L.total = off;
+  return L;
+}
+
+smd::ConvertParams convert_params(const smd_dims* d, const int32_t* bt, const int32_t* req,
+                                  const int32_t* topk, const int32_t* swa, int32_t* gidx, uint32_t* status) {
+  smd::ConvertParams p{};
+  p.block_table = bt;
+  p.req_id = req;
+  p.topk = topk;
+  p.swa = swa;
+  p.gidx = gidx;
+  p.status = status;
+  p.T = d->num_tokens;
+  p.R = d->num_requests;
+  p.max_blocks = d->max_blocks_per_req;
+  p.P = d->block_size;
+  p.K = d->topk;
+  p.W = d->swa;
+  p.num_pages = d->num_pages;
+  p.bt_stride = d->bt_stride;
+  p.topk_stride = d->topk_stride;
+  p.swa_stride = d->swa_stride;
+  return p;
+}
+
+int check_index_ptrs(const smd_dims* d, const int32_t* bt, const int32_t* req, const int32_t* topk,
+                     const int32_t* swa) {
+  if (d->num_tokens == 0) return SMD_OK;
+  if (bt == nullptr || req == nullptr) return fail(SMD_ERR_INVALID_ARG, "block_table and req_id are required");
+  if (d->topk > 0 && topk == nullptr) return fail(SMD_ERR_INVALID_ARG, "topk_idx is NULL with topk > 0");
+  if (d->swa > 0 && swa == nullptr) return fail(SMD_ERR_INVALID_ARG, "swa_idx is NULL with swa > 0");
+  return SMD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SMD_API const char* smd_last_error(void) { return g_err; }
+
+SMD_API int smd_version(void) { return 100; }
+
+SMD_API int smd_select_num_splits(const smd_dims* dims, int num_splits, int num_sms) {
+  g_err[0] = '\0';
+  const int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  if (num_splits < -SMD_MAX_SPLITS) return fail(SMD_ERR_INVALID_ARG, "num_splits %d < -%d", num_splits, SMD_MAX_SPLITS);
+  const int sms = device_sms(num_sms);
+  if (sms <= 0) return fail(SMD_ERR_CUDA, "cannot query the device SM count");
+  return select_splits(dims, num_splits, sms);
+}
+
+SMD_API size_t smd_workspace_size(const smd_dims* dims, int num_splits, int num_sms) {
+  const int S = smd_select_num_splits(dims, num_splits, num_sms);
+  if (S < 1) return 0;
+  return workspace_layout(dims, S).total;
+}
+
+SMD_API int smd_convert_req_index(const smd_dims* dims, const int32_t* block_table, const int32_t* req_id,
+                                  const int32_t* topk_idx, const int32_t* swa_idx, int32_t* gidx,
+                                  smd_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  rc = check_index_ptrs(dims, block_table, req_id, topk_idx, swa_idx);
+  if (rc != SMD_OK) return rc;
+  if (dims->num_tokens > 0 && dims->topk + dims->swa > 0 && gidx == nullptr)
+    return fail(SMD_ERR_INVALID_ARG, "gidx is NULL");
+  const cudaError_t e =
+      smd::launch_convert(convert_params(dims, block_table, req_id, topk_idx, swa_idx, gidx, nullptr), stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "convert launch");
+}
+
+SMD_API int smd_gather_dequant(const smd_dims* dims, const uint8_t* kv_cache, const int32_t* gidx,
+                               int64_t num_rows, void* kv_out, smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (dims == nullptr) return fail(SMD_ERR_INVALID_ARG, "dims is NULL");
+  if (dims->block_size < 1 || dims->num_pages < 1 || dims->num_pages > (int64_t)INT32_MAX / dims->block_size)
+    return fail(SMD_ERR_INVALID_ARG, "bad block_size/num_pages");
+  if (num_rows < 0) return fail(SMD_ERR_INVALID_ARG, "num_rows < 0");
+  if (num_rows == 0) return SMD_OK;
+  if (kv_cache == nullptr || gidx == nullptr || kv_out == nullptr)
+    return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(kv_cache) || !aligned16(kv_out)) return fail(SMD_ERR_INVALID_ARG, "kv_cache/kv_out not 16-byte aligned");
+  smd::GatherParams p{kv_cache, gidx, kv_out, num_rows, dims->num_pages, dims->block_size};
+  const cudaError_t e = smd::launch_gather_dequant(p, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "gather launch");
+}
+
+SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_heads, const float* o_part,
+                            const float* lse_part, const float* sink, void* out, float* lse, smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (num_tokens < 0 || num_heads < 1 || num_splits < 1 || num_splits > SMD_MAX_SPLITS)
+    return fail(SMD_ERR_INVALID_ARG, "bad combine shape T=%d S=%d H=%d", num_tokens, num_splits, num_heads);
+  if (num_tokens == 0) return SMD_OK;
+  if (o_part == nullptr || lse_part == nullptr || out == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(o_part) || !aligned16(out)) return fail(SMD_ERR_INVALID_ARG, "o_part/out not 16-byte aligned");
+  smd::CombineParams p{o_part, lse_part, sink, out, lse, num_tokens, num_splits, num_heads};
+  const cudaError_t e = smd::launch_combine(p, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "combine launch");
+}
+
+SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
+                                  const int32_t* block_table, const int32_t* req_id, const int32_t* topk_idx,
+                                  const int32_t* swa_idx, const float* sink, float scale, void* out, float* lse,
+                                  int num_splits, void* workspace, size_t workspace_bytes, smd_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  rc = check_index_ptrs(dims, block_table, req_id, topk_idx, swa_idx);
+  if (rc != SMD_OK) return rc;
+  if (num_splits < -SMD_MAX_SPLITS) return fail(SMD_ERR_INVALID_ARG, "num_splits %d < -%d", num_splits, SMD_MAX_SPLITS);
+  if (dims->num_tokens > 0) {
+    if (q == nullptr || kv_cache == nullptr || out == nullptr)
+      return fail(SMD_ERR_INVALID_ARG, "q, kv_cache and out are required");
+    if (!aligned16(q) || !aligned16(out) || !aligned16(kv_cache))
+      return fail(SMD_ERR_INVALID_ARG, "q/out/kv_cache not 16-byte aligned");
+  }
+  if (workspace == nullptr || !aligned16(workspace))
+    return fail(SMD_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+  const int sms = device_sms(0);
+  if (sms <= 0) return fail(SMD_ERR_CUDA, "cannot query the device SM count");
+  const int S = select_splits(dims, num_splits, sms);
+  const Layout L = workspace_layout(dims, S);
+  if (workspace_bytes < L.total)
+    return fail(SMD_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  int32_t* gidx = reinterpret_cast<int32_t*>(ws + L.gidx);
+
+  cudaError_t e = smd::launch_convert(
+      convert_params(dims, block_table, req_id, topk_idx, swa_idx, gidx, status), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "convert launch");
+  if (dims->num_tokens == 0) return SMD_OK;
+
+  const int64_t N = (int64_t)dims->topk + dims->swa;
+  const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
+  smd::AttnParams a{};
+  a.q = q;
+  a.cache = kv_cache;
+  a.gidx = gidx;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.o_part = S > 1 ? reinterpret_cast<float*>(ws + L.o_part) : nullptr;
+  a.lse_part = S > 1 ? reinterpret_cast<float*>(ws + L.lse_part) : nullptr;
+  a.status = status;
+  a.scale = scale;
+  a.num_pages = dims->num_pages;
+  a.T = dims->num_tokens;
+  a.H = dims->num_heads;
+  a.N = (int32_t)N;
+  a.P = dims->block_size;
+  a.S = S;
+  a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
+  if (a.tiles_per_split < 1) a.tiles_per_split = 1;
+  e = smd::launch_attn(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (S > 1) {
+    smd::CombineParams c{a.o_part, a.lse_part, sink, out, lse, dims->num_tokens, S, dims->num_heads};
+    e = smd::launch_combine(c, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return SMD_OK;
+}
+
+SMD_API int smd_read_status(const void* workspace, int32_t* device_status, smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (workspace == nullptr || device_status == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *device_status = v;
+  return v != 0 ? fail(SMD_ERR_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", v) : SMD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,239 @@
+// Device-side building blocks for libsmd (sm_103a): the fp8_ds_mla row format, the
+// row dequantiser, and thin inline-PTX wrappers for mbarrier, tcgen05 (TMEM
+// allocation, MMA, loads/stores, fences) and the UMMA descriptors.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace smd {
+
+// ---------------------------------------------------------------- row format
+// SGLang PR #26208 report, "关键源码片段": 448 fp8 NoPE + 64 bf16 RoPE = 576 data bytes,
+// 7 UE8M0 scales + 1 pad = 8 scale bytes; a page holds its data rows, then its scale rows.
+constexpr int kLatent = 512;
+constexpr int kNope = 448;
+constexpr int kRope = 64;
+constexpr int kGroup = 64;
+constexpr int kDataBytes = 576;
+constexpr int kScaleBytes = 8;
+constexpr int kRowBytes = kDataBytes + kScaleBytes;
+
+struct CacheView {
+  const uint8_t* base;
+  int64_t page_bytes;   // P * 584
+  int64_t scale_start;  // P * 576: offset of the scale rows inside a page
+  int32_t P;
+};
+
+__device__ __forceinline__ const uint8_t* row_data(const CacheView& c, int32_t slot) {
+  const int32_t page = slot / c.P;
+  const int32_t off = slot - page * c.P;
+  return c.base + (int64_t)page * c.page_bytes + (int64_t)off * kDataBytes;
+}
+__device__ __forceinline__ const uint8_t* row_scales(const CacheView& c, int32_t slot) {
+  const int32_t page = slot / c.P;
+  const int32_t off = slot - page * c.P;
+  return c.base + (int64_t)page * c.page_bytes + c.scale_start + (int64_t)off * kScaleBytes;
+}
+
+// 2^(code-127) as an fp32 bit pattern; code 0 is the subnormal 2^-127 and code 255
+// becomes +inf, which the scrub below turns into 0 for every element it scales.
+__device__ __forceinline__ float ue8m0_to_float(uint32_t code) {
+  return code == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(code << 23);
+}
+
+// Zero every bf16 lane whose exponent field is all ones (inf or NaN).
+__device__ __forceinline__ uint32_t scrub_bf16x2(uint32_t v) {
+  const uint32_t bad = __vcmpeq2(v & 0x7F807F80u, 0x7F807F80u);
+  return v & ~bad;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 bytes (low byte = lower element) times a power-of-two scale -> scrubbed bf16x2.
+// fp8 -> fp16 is exact for every e4m3 value; the fp32 product is exact unless it
+// overflows; the bf16 rounding is exact whenever the product stays in bf16's normal
+// range, so the result equals the exactly-rounded latent value.
+__device__ __forceinline__ uint32_t dequant_fp8x2(uint16_t two, float scale) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  return scrub_bf16x2(bf16x2_bits(__floats2bfloat162_rn(f.x * scale, f.y * scale)));
+}
+
+// 16 fp8 bytes (uint4) -> 16 bf16 (two uint4), one scale for all.
+__device__ __forceinline__ void dequant16(const uint4 in, float scale, uint4& lo, uint4& hi) {
+  lo.x = dequant_fp8x2((uint16_t)(in.x & 0xFFFF), scale);
+  lo.y = dequant_fp8x2((uint16_t)(in.x >> 16), scale);
+  lo.z = dequant_fp8x2((uint16_t)(in.y & 0xFFFF), scale);
+  lo.w = dequant_fp8x2((uint16_t)(in.y >> 16), scale);
+  hi.x = dequant_fp8x2((uint16_t)(in.z & 0xFFFF), scale);
+  hi.y = dequant_fp8x2((uint16_t)(in.z >> 16), scale);
+  hi.z = dequant_fp8x2((uint16_t)(in.w & 0xFFFF), scale);
+  hi.w = dequant_fp8x2((uint16_t)(in.w >> 16), scale);
+}
+
+__device__ __forceinline__ uint4 scrub_bf16x8(uint4 v) {
+  v.x = scrub_bf16x2(v.x);
+  v.y = scrub_bf16x2(v.y);
+  v.z = scrub_bf16x2(v.z);
+  v.w = scrub_bf16x2(v.w);
+  return v;
+}
+
+// 16-byte global load; ALIGN16 = false splits it into two 8-byte loads (pages with an
+// odd slot count leave data rows only 8-byte aligned).
+template <bool ALIGN16>
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
+  if constexpr (ALIGN16) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  } else {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(p + 8));
+    return make_uint4(a.x, a.y, b.x, b.y);
+  }
+}
+
+// ---------------------------------------------------------------- misc PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after `limit_ns` of wall time and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the async proxy (UMMA operand reads).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, f32 accumulate).
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive (once) on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w reads lanes 32w..32w+31).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// UMMA shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
+// start >> 4 in bits [0,14), leading-dimension byte offset >> 4 in [16,30), stride-
+// dimension byte offset >> 4 in [32,46), version 1 in [46,48), swizzle mode 2 in [61,64)).
+// The tile base must be 1024-byte aligned (base-offset field 0).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulator.
+// a_mn / b_mn select MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                          // D format: f32
+         | (1u << 7)                        // A format: bf16
+         | (1u << 10)                       // B format: bf16
+         | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17)         // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled slab
+// whose rows are 128 bytes apart (8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+}  // namespace smd

@@ -1,0 +1,61 @@
+// Internal launch interface between the C-ABI layer (smd_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace smd {
+
+constexpr int kTileRows = 64;     // gathered rows per attention tile
+constexpr int kMaxSplits = 32;
+
+struct ConvertParams {
+  const int32_t* block_table;
+  const int32_t* req_id;
+  const int32_t* topk;
+  const int32_t* swa;
+  int32_t* gidx;          // [T, K+W]
+  uint32_t* status;       // reset to 0 by the launch when non-null
+  int32_t T, R, max_blocks, P, K, W;
+  int64_t num_pages, bt_stride, topk_stride, swa_stride;
+};
+cudaError_t launch_convert(const ConvertParams& p, cudaStream_t s);
+
+struct GatherParams {
+  const uint8_t* cache;
+  const int32_t* gidx;
+  void* kv_out;           // bf16 [rows, 512]
+  int64_t rows, num_pages;
+  int32_t P;
+};
+cudaError_t launch_gather_dequant(const GatherParams& p, cudaStream_t s);
+
+struct CombineParams {
+  const float* o_part;    // [T, S, H, 512]
+  const float* lse_part;  // [T, S, H]
+  const float* sink;      // [H] or null
+  void* out;              // bf16 [T, H, 512]
+  float* lse;             // [T, H] or null
+  int32_t T, S, H;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+struct AttnParams {
+  const void* q;          // bf16 [T, H, 512]
+  const uint8_t* cache;
+  const int32_t* gidx;    // [T, N] converted slots, -1 = masked
+  const float* sink;      // [H] or null
+  void* out;              // bf16 [T, H, 512]          (S == 1)
+  float* lse;             // [T, H] or null            (S == 1)
+  float* o_part;          // [T, S, H, 512]            (S > 1)
+  float* lse_part;        // [T, S, H]                 (S > 1)
+  uint32_t* status;       // device status word
+  float scale;
+  int64_t num_pages;
+  int32_t T, H, N, P, S;
+  int32_t tiles_per_split;
+};
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
+int attn_ctas_per_split();
+
+}  // namespace smd

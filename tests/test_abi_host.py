@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+function include/smd.h declares, and its host-only logic (split selector, workspace
+size, argument validation) behaves as documented."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sparse_mla_decode_req_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load()
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "smd.h")).read()
+    return re.findall(r"SMD_API\s+[\w\s\*]+?\b(smd_\w+)\s*\(", txt)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(api._SIGS), "binding signatures must mirror the header"
+
+
+def test_only_abi_symbols_are_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", api.lib_path()], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("smd_")}
+    assert ours == set(_declared())
+
+
+def _dims(T=4, H=128, K=2048, W=128, P=64, pages=8192, R=4, B=2048):
+    return api.Dims(num_tokens=T, num_heads=H, num_requests=R, max_blocks_per_req=B, num_pages=pages,
+                    block_size=P, topk=K, swa=W, pad_=0, bt_stride=B, topk_stride=K, swa_stride=W)
+
+
+def test_split_selector_rules(lib):
+    # forced counts are honoured exactly
+    for s in (1, 2, 7, 32):
+        assert api.select_num_splits(_dims(), -s, 152) == s
+    # caps are honoured
+    for cap in (1, 2, 8, 32):
+        assert 1 <= api.select_num_splits(_dims(), cap, 152) <= cap
+    # short work (<= 1024 entries) never exceeds 4 splits
+    assert api.select_num_splits(_dims(T=1, H=64, K=512, W=128), 0, 152) <= 4
+    # long context, low batch: the selector uses many splits to fill the GPU
+    s4 = api.select_num_splits(_dims(), 32, 152)
+    assert 8 <= s4 <= 32
+    # large batch fills the GPU without splitting
+    assert api.select_num_splits(_dims(T=256, H=64, K=512, W=128), 0, 152) == 1
+    # every split keeps at least one 64-row tile
+    for T in (1, 2, 3, 5, 16):
+        for N in (1, 63, 64, 65, 200, 640, 2176):
+            d = _dims(T=T, K=N, W=0)
+            s = api.select_num_splits(d, 0, 152)
+            tiles = -(-N // 64)
+            tps = -(-tiles // s)
+            assert (s - 1) * tps < tiles
+    # depends on shapes and SM count only (graph-safe): repeatable
+    assert api.select_num_splits(_dims(), 0, 152) == api.select_num_splits(_dims(), 0, 152)
+
+
+def test_workspace_size_layout(lib):
+    d = _dims(T=4, H=128, K=2048, W=128)
+    s = api.select_num_splits(d, -8, 152)
+    n = api.workspace_size(d, -8, 152)
+    T, N, H = 4, 2176, 128
+    need = 256 + T * N * 4 + T * s * H * 512 * 4 + T * s * H * 4
+    assert need <= n <= need + 3 * 256
+    d1 = _dims(T=256, H=64, K=512, W=128)
+    assert api.workspace_size(d1, 1, 152) == 256 + ((256 * 640 * 4 + 255) // 256) * 256
+
+
+@pytest.mark.parametrize("field,value", [("num_heads", 0), ("num_heads", 129), ("block_size", 0),
+                                         ("num_pages", 0), ("topk", -1), ("bt_stride", 1),
+                                         ("num_tokens", -1), ("num_tokens", 70000)])
+def test_invalid_dims_rejected_before_any_launch(lib, field, value):
+    d = _dims()
+    setattr(d, field, value)
+    rc = lib.smd_select_num_splits(ctypes.byref(d), 0, 152)
+    assert rc == api.SMD_ERR_INVALID_ARG
+    assert api.last_error()
+    ws = ctypes.create_string_buffer(64)
+    rc = lib.smd_sparse_mla_decode(ctypes.byref(d), None, None, None, None, None, None, None, 1.0, None,
+                                   None, 0, ws, 64, None)
+    assert rc == api.SMD_ERR_INVALID_ARG
+
+
+def test_null_pointers_rejected(lib):
+    d = _dims(T=2)
+    rc = lib.smd_convert_req_index(ctypes.byref(d), None, None, None, None, None, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "required" in api.last_error()
+    rc = lib.smd_lse_combine(2, 0, 4, None, None, None, None, None, None)
+    assert rc == api.SMD_ERR_INVALID_ARG
+    rc = lib.smd_gather_dequant(ctypes.byref(d), None, None, 5, None, None)
+    assert rc == api.SMD_ERR_INVALID_ARG
+    v = ctypes.c_int32(0)
+    assert lib.smd_read_status(None, ctypes.byref(v), None) == api.SMD_ERR_INVALID_ARG
+
+
+def test_version(lib):
+    assert lib.smd_version() >= 100
