@@ -196,7 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(AttnParams p)
     for (int ch = 0; ch < 8; ++ch)
       *reinterpret_cast<uint4*>(sP + sw128_off(tid, ch)) =
           make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-    if (o_live && alpha != 1.f) {  // rescale this lane's 256 accumulator columns
+    // Rescale the 256 accumulator columns when any lane of the warp needs it: tcgen05.ld/st
+    // are warp-collective, so the branch must be warp-uniform (lanes with alpha == 1
+    // rewrite their values unchanged).
+    const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+    if (o_live && rescale) {
 #pragma unroll 1
       for (int cc = 0; cc < kDHalf / 32; ++cc) {
         uint32_t o[32];
