@@ -1,0 +1,410 @@
+#!/usr/bin/env python3
+"""Benchmark one sparse MLA decode step on synthetic fp8_ds_mla inputs; prints ONE JSON line.
+
+Metric: gathered KV tokens/s (valid (token, entry) rows attended per second) for one
+decode step = index conversion + fused gather/dequant/tcgen05 attention + LSE combine,
+all in libsmd's CUDA kernels.  Inputs are resident in HBM when the timed region starts;
+L2 is flushed (a 512 MiB write) between timed steps, outside the per-step CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+--config picks one of the five decode workloads (0 tiny, 1 single request [default],
+2 mid batch, 3 large batch, 4 long context).  Under torchrun each rank runs its own
+replica of the workload on its own GPU (weak scaling, no data-path collective); the
+timed region is bracketed by barriers and the max time over ranks is reported.
+``--impl reference`` times the float64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "gathered KV tokens/s and achieved HBM GB/s (fraction of roofline) per decode step"
+UNIT = "tokens/s"
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample length")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline(H: int, rows: int, seconds: float, peaks: dict, source: str, traffic=None) -> dict:
+    """Roofline of the attention kernel: 584 gathered bytes and 4*512*H flops per valid row."""
+    bytes_ = 584.0 * rows
+    flops = 4.0 * 512 * H * rows
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    gbs = bytes_ / seconds / 1e9
+    tflops = flops / seconds / 1e12
+    if flops / bytes_ > ridge:
+        r = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["traffic"] = traffic
+    r["peak_source"] = f"{source} (MEASURED_PEAKS.json burst)" if source == "measured" else "fallback"
+    r["algorithmic_bytes_per_launch"] = bytes_
+    r["algorithmic_flops_per_launch"] = flops
+    r["hbm_gbs_achieved"] = gbs
+    r["hbm_frac"] = gbs / peaks["hbm_gbs"]
+    r["tensor_tflops_achieved"] = tflops
+    r["tensor_frac"] = tflops / peaks["bf16_tflops"]
+    return r
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i",
+                 str(self.index), "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_rate(inp, seconds: float, max_steps: int | None = None):
+    """Time the float64 oracle on whole tokens of the workload (cycling) for ~`seconds`."""
+    import numpy as np
+
+    import oracle
+    w = inp.workload
+    q = oracle.decode_bf16(inp.q.cpu().contiguous().view(__import__("torch").int16).numpy().view(np.uint16))
+    cache = inp.kv_cache.cpu().numpy()
+    bt = inp.block_table.cpu().numpy()
+    rid = inp.req_id.cpu().numpy()
+    topk = inp.topk_idx.cpu().numpy()
+    swa = inp.swa_idx.cpu().numpy()
+    sink = inp.sink.cpu().double().numpy()
+    valid = ((topk >= 0).sum(axis=1) + (swa >= 0).sum(axis=1)) if w.n_entries else np.zeros(w.num_tokens)
+    rows = 0
+    steps = 0
+    t0 = time.perf_counter()
+    t = 0
+    while True:
+        oracle.sparse_mla_decode(q, cache, bt, rid, topk, swa, sink, inp.scale, w.block_size, tokens=[t])
+        rows += int(valid[t])
+        steps += 1
+        t = (t + 1) % w.num_tokens
+        el = time.perf_counter() - t0
+        if (max_steps is not None and steps >= max_steps) or (max_steps is None and el >= seconds):
+            break
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return rows / el, el, steps, rows, cores
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the float64 CPU oracle, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import torch
+
+    from sparse_mla_decode_req_gb300 import synth
+    w = synth.WORKLOADS[args.config]
+    inp = synth.make_inputs(w, device="cpu")
+    cpu_oracle_rate(inp, 0.0, max_steps=max(1, args.warmup))
+    rate, el, steps, rows, cores = cpu_oracle_rate(inp, 0.0, max_steps=max(1, args.steps))
+    sample = f"{steps} oracle steps of one token each (cycling over the {w.num_tokens} tokens), {rows} valid rows"
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, None),
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    del torch
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, splits):
+    return {"workload": w.name, "description": w.description, "batch": w.num_tokens, "heads": w.num_heads,
+            "topk": w.topk, "swa": w.swa, "context": [w.ctx_lo, w.ctx_hi], "block_size": w.block_size,
+            "splits": splits, "l2": "flushed between timed steps (512 MiB write)"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import ctypes
+
+    import torch
+
+    from sparse_mla_decode_req_gb300 import api, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    lib = api.load()
+    w = synth.WORKLOADS[args.config]
+    seed = synth.SEED_BASE + args.config + 1000 * rank
+    inp = synth.make_inputs(w, seed=seed, device=dev)
+    T, H, N = w.num_tokens, w.num_heads, w.n_entries
+    rows_per_step = inp.n_valid
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    dims = api.make_dims(inp.q, inp.kv_cache, inp.block_table, inp.req_id,
+                         inp.topk_idx if w.topk else None, inp.swa_idx if w.swa else None, w.block_size)
+    S = api.select_num_splits(dims, w.max_splits, sms)
+    topk = inp.topk_idx if w.topk else None
+    swa = inp.swa_idx if w.swa else None
+
+    # buffers of the staged step
+    gidx = torch.empty(T, N, dtype=torch.int32, device=dev)
+    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    o_part = torch.empty(T, S, H, 512, dtype=torch.float32, device=dev) if S > 1 else None
+    lse_part = torch.empty(T, S, H, dtype=torch.float32, device=dev) if S > 1 else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = api._ptr
+    conv_args = (ctypes.byref(dims), P(inp.block_table), P(inp.req_id), P(topk), P(swa), P(gidx), sp)
+    attn_dims = api.Dims(num_tokens=T, num_heads=H, num_requests=1, max_blocks_per_req=1,
+                         num_pages=inp.num_pages, block_size=w.block_size, topk=N, swa=0, pad_=0, bt_stride=1,
+                         topk_stride=max(N, 1), swa_stride=0)
+    attn_args = (ctypes.byref(attn_dims), P(inp.q), P(inp.kv_cache), P(gidx), P(inp.sink),
+                 ctypes.c_float(inp.scale), int(w.max_splits), P(out), P(lse), P(o_part), P(lse_part),
+                 P(status), sp)
+    comb_args = (T, S, H, P(o_part), P(lse_part), P(inp.sink), P(out), P(lse), sp)
+
+    def step():
+        api._check(lib.smd_convert_req_index(*conv_args))
+        api._check(lib.smd_sparse_mla_attention(*attn_args))
+        if S > 1:
+            api._check(lib.smd_lse_combine(*comb_args))
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.1)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        api._check(lib.smd_convert_req_index(*conv_args))
+        e[1].record(stream)
+        api._check(lib.smd_sparse_mla_attention(*attn_args))
+        e[2].record(stream)
+        if S > 1:
+            api._check(lib.smd_lse_combine(*comb_args))
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    conv_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_s = sum(step_ms) / 1e3
+    if pg is not None:
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_s = float(t.item())
+    assert int(status.item()) == 0, "a kernel's bounded wait gave up during the benchmark"
+    value = rows_per_step * K * world / total_s
+    ms_per_step = total_s / K * 1e3
+
+    peaks, src = load_peaks()
+    traffic = load_traffic(w.name)
+    roof = roofline(H, rows_per_step, statistics.mean(attn_ms) / 1e3, peaks, src, traffic)
+    roof["kernel"] = "smd::attn_partial_kernel"
+    roof["launch_ms_mean"] = statistics.mean(attn_ms)
+
+    # end to end through the public call with host buffers: h2d of the step's inputs,
+    # decode, d2h of out + lse, per step
+    e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step)
+    if pg is not None:
+        t = torch.tensor([e2e["seconds"]], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e["seconds"] = float(t.item())
+    e2e_val = rows_per_step * e2e["steps"] * world / e2e["seconds"]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, el, steps_done, rows_done, cores = cpu_oracle_rate(inp, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{steps_done} oracle steps of one token each ({rows_done} valid rows, {el:.1f} s, "
+                         f"numpy BLAS on all host cores)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; fp8_ds_mla rows quantised from N(0,1))",
+        "config": workload_config(w, S),
+        "roofline": roof,
+        "step_breakdown_ms": {"convert": statistics.mean(conv_ms), "attention": statistics.mean(attn_ms),
+                              "combine": statistics.mean(comb_ms) if S > 1 else 0.0},
+        "hbm_gbs_step": 584.0 * rows_per_step / (ms_per_step / 1e3) / 1e9,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "steps": e2e["steps"]},
+        "gpu_launches": K * (2 + (1 if S > 1 else 0)),
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def load_traffic(name: str):
+    """DRAM bytes per attention launch from a committed ncu summary, if the kernel is unchanged."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    src = os.path.join(ROOT, "sparse_mla_decode_req_gb300", "csrc", "k_attn.cu")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        e = d.get(name)
+        if e and e.get("k_attn_sha") == sha:
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step):
+    import torch
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("q", "block_table", "req_id", "topk_idx", "swa_idx")}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    T, H = w.num_tokens, w.num_heads
+    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    h_out = torch.empty(T, H, 512, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    dims = api.make_dims(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
+                         dbuf["topk_idx"] if w.topk else None, dbuf["swa_idx"] if w.swa else None, w.block_size)
+    ws = torch.empty(api.workspace_size(dims, w.max_splits, 0), dtype=torch.uint8, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def one():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        api.sparse_mla_decode(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
+                              dbuf["topk_idx"] if w.topk else None, dbuf["swa_idx"] if w.swa else None,
+                              inp.sink, inp.scale, out=out, lse=lse, num_splits=w.max_splits, workspace=ws,
+                              block_size=w.block_size)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    secs = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    return {"seconds": secs, "steps": steps, "h2d": h2d, "d2h": d2h}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

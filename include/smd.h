@@ -138,6 +138,23 @@ SMD_API int smd_sparse_mla_decode(const smd_dims *dims, const void *q, const uin
                                   smd_stream_t stream);
 
 /*
+ * Steps 2-4 alone, for already-converted slots: the fused gather + dequant + tcgen05
+ * attention kernel over gidx i32 [T, K+W] as written by smd_convert_req_index (entries
+ * < 0 or >= num_pages * block_size are masked).  The split count S follows num_splits as
+ * for smd_select_num_splits (current device's SM count).  S == 1: writes out bf16
+ * [T, H, 512] and lse f32 [T, H] (lse may be NULL) with the sink in the denominator.
+ * S > 1: writes each split's normalised output o_part f32 [T, S, H, 512] and its
+ * sink-free lse_part f32 [T, S, H] (-inf for a split without valid entries), to be
+ * merged by smd_lse_combine; out/lse are not touched.  status (optional, device int32)
+ * gets bit 0 set if a bounded wait inside the kernel gives up.  dims->topk + dims->swa is
+ * the row length of gidx; the index pointers of dims are not used.
+ */
+SMD_API int smd_sparse_mla_attention(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
+                                     const int32_t *gidx, const float *sink, float scale, int num_splits,
+                                     void *out, float *lse, float *o_part, float *lse_part,
+                                     int32_t *status, smd_stream_t stream);
+
+/*
  * Step 1 alone: writes gidx i32 [T, K+W] (top-k entries first, window entries at
  * offset K) with the global slot of each valid entry and -1 for every invalid one
  * (index < 0, block outside [0, max_blocks), page outside [0, num_pages), request id

