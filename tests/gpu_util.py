@@ -10,6 +10,10 @@ from sparse_mla_decode_req_gb300 import synth
 OUT_MAX_ABS = 2e-2
 OUT_MEAN_REL = 5e-3
 LSE_MAX_ABS = 1e-3
+# plus a relative part: fp32 accumulation of a 512-term dot product carries a relative
+# error of order 512 * 2^-24 ~ 3e-5 of the score magnitude, which dominates when one
+# row's scores are huge (lse ~ 1e12 in the large-scale-code poison case)
+LSE_REL = 3e-5
 
 
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -50,5 +54,7 @@ def assert_lse_close(lse_gpu: torch.Tensor, ref: np.ndarray, what=""):
     assert np.array_equal(np.isneginf(got), inf_ref), f"{what}: -inf pattern differs"
     fin = ~inf_ref
     if fin.any():
-        err = float(np.abs(got[fin] - ref[fin]).max())
-        assert err <= LSE_MAX_ABS, f"{what}: lse max abs error {err:.3e}"
+        err = np.abs(got[fin] - ref[fin])
+        tol = LSE_MAX_ABS + LSE_REL * np.abs(ref[fin])
+        worst = int(np.argmax(err - tol))
+        assert np.all(err <= tol), f"{what}: lse error {err[worst]:.3e} > {tol[worst]:.3e}"
