@@ -191,6 +191,32 @@ SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_
  */
 SMD_API int smd_read_status(const void *workspace, int32_t *device_status, smd_stream_t stream);
 
+/*
+ * Allocation-free variant of smd_sparse_mla_decode.  The pages have no counterpart: it
+ * exists for callers that cannot allocate device memory -- a serving engine that gave
+ * nearly all HBM to its paged KV cache at start-up and forbids further cudaMalloc, a
+ * plugin living inside a process whose allocator owns the device, or a latency-critical
+ * path that cannot take cudaMalloc's implicit device synchronisation.
+ *
+ * Same arguments and results as smd_sparse_mla_decode, minus the workspace: the scratch
+ * (status word, converted slots, split partials) is a static device array of
+ * SMD_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * holds until the process exits.  A step whose scratch need (smd_workspace_size) exceeds
+ * that size is rejected with SMD_ERR_WORKSPACE and a message; nothing is launched.
+ * The call allocates nothing.  Its first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls on a device share the one array and it keeps the last
+ * call's contents (the call resets the status word itself and overwrites everything else
+ * it reads), so calls whose kernels overlap on the GPU -- e.g. on two streams without an
+ * ordering between them -- race on the scratch.  Serialise them.
+ */
+#define SMD_STATIC_SCRATCH_BYTES (32u << 20)
+SMD_API int smd_sparse_mla_decode_static_scratch(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
+                                                 const int32_t *block_table, const int32_t *req_id,
+                                                 const int32_t *topk_idx, const int32_t *swa_idx,
+                                                 const float *sink, float scale, void *out, float *lse,
+                                                 int num_splits, smd_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 SMD_API const char *smd_last_error(void);
 

@@ -65,6 +65,8 @@ _SIGS = {
     "smd_convert_req_index": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P]),
     "smd_gather_dequant": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, ctypes.c_int64, _P, _P]),
     "smd_lse_combine": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P]),
+    "smd_sparse_mla_decode_static_scratch": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P, _P,
+                                                            ctypes.c_float, _P, _P, ctypes.c_int, _P]),
     "smd_read_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "smd_last_error": (ctypes.c_char_p, []),
     "smd_version": (ctypes.c_int, []),

@@ -154,6 +154,16 @@ int check_index_ptrs(const smd_dims* d, const int32_t* bt, const int32_t* req, c
 
 }  // namespace
 
+namespace smd {
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+}  // namespace smd
+
 extern "C" {
 
 SMD_API const char* smd_last_error(void) { return g_err; }

@@ -58,4 +58,7 @@ struct AttnParams {
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
 int attn_ctas_per_split();
 
+// Sets the thread-local message returned by smd_last_error() and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 }  // namespace smd
