@@ -2,322 +2,499 @@
 //
 // What it computes (vLLM PR #52212 report, "实现拆解" item 1; SGLang PR #26208 report,
 // _unified_sparse_decode_kernel interface Q, KV, Mask, AttnSink, Output, LSE, sm_scale):
-// for token t and split s, over the split's gathered entries e (64-row tiles of the
+// for token t and split s, over the split's gathered entries e (128-row tiles of the
 // converted slot list), s[h,e] = scale * q[t,h,:] . k_e with one 512-wide dot for all
 // heads, invalid entries masked, online softmax, o[h,:] = sum_e p[h,e] k_e over the same
-// 512-wide latent (K = V).  One split: the sink logit joins the denominator here and
-// bf16 out + lse are written directly.  Several splits: the split's normalised o and
-// its lse (no sink) go to the workspace for the combine kernel.
+// 512-wide latent (K = V).  One split: the sink logit joins the denominator and bf16 out
+// + lse are written directly.  Several splits: the split's normalised o and its lse (no
+// sink) go to the workspace for the combine kernel.
 //
-// GB300 mapping.  Heads are the MMA M dimension (zero-padded to 128).  O = 128 x 512
-// fp32 would fill all 512 TMEM columns, so each (token, split) is handled by two CTAs
-// that own latent dims [0,256) and [256,512) of the output: each computes the full
-// 512-wide QK tile into TMEM (S, 64 columns), runs the softmax in registers (thread h =
-// TMEM lane h = head h), writes P (bf16) to shared memory and accumulates its half of O
-// (256 TMEM columns) with a second UMMA that reads the same dequantised tile as an
-// MN-major B operand.  The gather uses 16-byte vector loads; the dequantised tile is
-// written straight into the 128-byte-swizzled UMMA layout.
+// GB300 mapping.  Heads are the UMMA M dimension (zero-padded to 128; M = 64 UMMAs run
+// at half rate on this part, so nothing is lost by padding).  The O accumulator of 128
+// heads x 512 dims in fp32 would fill all 512 TMEM columns, so a (token, split) is owned
+// by a cluster of two CTAs, CTA c holding latent dims [256c, 256c+256) of K/V and of O:
+//
+//   TMEM (per CTA, 512 columns): Q half [0,128) as the A operand of QK (bf16 pairs),
+//   S partial / P [128,256) (P overwrites S as bf16 pairs), O half [256,512).
+//   SMEM: 2 stages x [128 rows x 256 dims] bf16 (128B-swizzled, 64 KB each) and a 64 KB
+//   buffer that receives the peer's partial scores.
+//
+// Per 128-row tile: producer warps gather the CTA's half of each 584-byte row with
+// 16-byte loads and dequantise it into the swizzled stage; the UMMA warp runs
+// S_c = Q_c K_c^T (M128 N128 K256, A from TMEM); the softmax warps (thread h = TMEM lane
+// h = head h) load S_c, send it to the peer over DSMEM, add the peer's partial, so both
+// CTAs hold the same full 512-wide scores, run the online softmax and write P back into
+// TMEM; the UMMA warp then runs O_c += P V_c (M128 N256 K128, A from TMEM, the same stage
+// read MN-major).  Every QK flop is done once across the pair.  The running max is only
+// moved when it grows by more than 2^8, so the O accumulator is rarely rescaled.
+//
+// Roles: warps 0-7 softmax + epilogue (two threads per head, 64 score columns each;
+// thread 0 also issues the UMMAs and warp 0 owns the TMEM allocation), warps 8-11
+// gather/dequant.  Every wait is bounded; a wait that gives up records bit 0 in the
+// status word and the CTA winds down (draining its UMMAs, freeing TMEM).
 #include "smd_device.cuh"
 #include "smd_internal.h"
 
 namespace smd {
 namespace {
 
-constexpr int kM = 128;          // MMA M: heads, zero-padded
-constexpr int kThreads = 128;    // thread h <-> TMEM lane h
-constexpr int kDHalf = 256;      // output dims per CTA
-constexpr uint32_t kQSlab = kM * 128;          // [128 rows x 64 dims] bf16 = 16 KB
-constexpr uint32_t kKSlab = kTileRows * 128;   // [64 rows x 64 dims] bf16 = 8 KB
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + 8 * kQSlab;           // 128 KB
-constexpr uint32_t kOffP = kOffK + 8 * kKSlab;           // +64 KB
-constexpr uint32_t kOffMisc = kOffP + kM * 128;          // +16 KB
-constexpr uint32_t kSmemBytes = kOffMisc + 512 + 1024;   // misc + alignment slack
+constexpr int kTile = kTileRows;            // 128 gathered rows per tile
+constexpr int kDHalf = 256;                 // latent dims per CTA
+constexpr int kStages = 2;
+constexpr int kSoftmaxThreads = 256;   // warps 0-7
+constexpr int kThreads = kSoftmaxThreads + 128;  // + producer warps 8-11
+constexpr uint32_t kSlab = kTile * 128;     // [128 rows x 64 dims] bf16 = 16 KB
+constexpr uint32_t kStageBytes = 4 * kSlab; // 64 KB
+constexpr uint32_t kXchgBytes = 128 * 128 * 4;
+constexpr uint32_t kOffXchg = kStages * kStageBytes;
+constexpr uint32_t kOffMisc = kOffXchg + kXchgBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
 struct Misc {
-  uint64_t mma_bar;
+  uint64_t kfull[kStages];   // producers -> UMMA: stage filled (128 arrivals)
+  uint64_t kempty[kStages];  // UMMA commit -> producers: stage consumed by PV
+  uint64_t sfull;            // UMMA commit -> softmax: S partial ready
+  uint64_t pfull;            // softmax -> issuer: P in TMEM, O rescaled (256 arrivals)
+  uint64_t xfull;            // peer softmax -> softmax: peer partial in xchg (256 remote arrivals)
+  uint64_t xempty;           // peer softmax -> softmax: peer drained our writes (256 remote arrivals)
+  uint64_t odone;            // issuer commit -> softmax: every PV done
+  uint64_t drain;            // UMMA self-drain before TMEM is freed after a failed wait
+  uint64_t sgrp;             // softmax-group rendezvous (256 arrivals per use)
+  uint64_t pgrp;             // producer-group rendezvous (128 arrivals per use)
   uint32_t tmem_base;
-  uint32_t pad;
-  int32_t slot[kTileRows];
+  uint32_t abort;
+  uint32_t mask[kStages][4];        // valid-row bit masks of the staged tile
+  int32_t slot[kStages][kTile];     // converted slots of the staged tile
+  float red_max[kStages][2][128];   // per-column-half tile maxima of each head
+  float red_sum[2][128];            // per-column-half denominators at the end
 };
+constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
 __device__ __forceinline__ float ex2(float x) { return exp2f(x); }
+
+__device__ __forceinline__ bool aborted(const Misc* m) {
+  return *reinterpret_cast<const volatile uint32_t*>(&m->abort) != 0u;
+}
+
+// Bounded wait that also gives up early once another role of this CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Misc* m,
+                                         bool cluster_acquire = false) {
+  auto poll = [&]() { return cluster_acquire ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!poll()) {
+    if (aborted(m) || globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void record_abort(Misc* m, uint32_t* status) {
+  atomicExch(&m->abort, 1u);
+  if (status != nullptr) atomicOr(status, 1u);
+}
+
+// Byte offset of the 16-byte chunk holding local dims [d0, d0+8) of `row` in a stage
+// made of four 128B-swizzled [128 rows x 64 dims] slabs.
+__device__ __forceinline__ uint32_t stage_off(uint32_t row, uint32_t d0) {
+  return (d0 >> 6) * kSlab + sw128_off(row, (d0 & 63) >> 3);
+}
+
+// Gather + dequantise this CTA's half of 128 rows into stage `st`.  Half 0: NoPE bytes
+// [0,256) with scale codes 0..3.  Half 1: NoPE bytes [256,448) with codes 4..6, then the
+// 64 RoPE values.  Consecutive threads take consecutive 16-byte chunks of a row, so each
+// warp load instruction reads whole contiguous row segments; all loads are issued before
+// the first conversion so they overlap in flight.
+template <int HALF, bool ALIGN16>
+__device__ __forceinline__ void fill_stage(uint8_t* st, const int32_t* slots, const CacheView& cv, int ptid) {
+  constexpr int NC = HALF == 0 ? 16 : 20;  // 16-byte input chunks per row
+  uint4 raw[NC];
+  uint32_t code[NC];
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const int k = i * 128 + ptid;
+    const int row = k / NC, ch = k - (k / NC) * NC;
+    const int32_t g = slots[row];
+    raw[i] = make_uint4(0, 0, 0, 0);
+    code[i] = 0;
+    if (g >= 0) {
+      const uint8_t* d = row_data(cv, g);
+      if (HALF == 0) {
+        raw[i] = ldg16<ALIGN16>(d + ch * 16);
+        code[i] = __ldg(row_scales(cv, g) + (ch >> 2));
+      } else if (ch < 12) {
+        raw[i] = ldg16<ALIGN16>(d + 256 + ch * 16);
+        code[i] = __ldg(row_scales(cv, g) + 4 + (ch >> 2));
+      } else {
+        raw[i] = ldg16<ALIGN16>(d + kNope + (ch - 12) * 16);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const int k = i * 128 + ptid;
+    const int row = k / NC, ch = k - (k / NC) * NC;
+    const bool valid = slots[row] >= 0;
+    if (HALF == 1 && ch >= 12) {
+      const uint4 v = valid ? scrub_bf16x8(raw[i]) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(st + stage_off(row, 192 + (ch - 12) * 8)) = v;
+    } else {
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (valid) dequant16(raw[i], ue8m0_to_float(code[i]), lo, hi);
+      *reinterpret_cast<uint4*>(st + stage_off(row, ch * 16)) = lo;
+      *reinterpret_cast<uint4*>(st + stage_off(row, ch * 16 + 8)) = hi;
+    }
+  }
+}
 
 }  // namespace
 
 template <bool ALIGN16>
-__global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(AttnParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pair_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + kOffQ;
-  uint8_t* sK = smem + kOffK;
-  uint8_t* sP = smem + kOffP;
-  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  uint8_t* xchg = smem + kOffXchg;
+  Misc* m = reinterpret_cast<Misc*>(smem + kOffMisc);
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int half = blockIdx.x & 1;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t half = cluster_rank();   // == blockIdx.x & 1
+  const uint32_t peer = half ^ 1u;
   const int split = blockIdx.x >> 1;
   const int t = blockIdx.y;
   const int N = p.N;
-  const int n_tiles = (N + kTileRows - 1) / kTileRows;
+  const int n_tiles_tok = (N + kTile - 1) / kTile;
   const int tile_begin = split * p.tiles_per_split;
-  const int tile_end = min(n_tiles, tile_begin + p.tiles_per_split);
+  const int n = max(0, min(n_tiles_tok, tile_begin + p.tiles_per_split) - tile_begin);
 
-  if (warp == 0) {
-    tmem_alloc(&misc->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
   if (tid == 0) {
-    mbar_init(&misc->mma_bar, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&m->kfull[s], 128);
+      mbar_init(&m->kempty[s], 1);
+    }
+    mbar_init(&m->sfull, 1);
+    mbar_init(&m->pfull, kSoftmaxThreads);
+    mbar_init(&m->xfull, kSoftmaxThreads);
+    mbar_init(&m->xempty, kSoftmaxThreads);
+    mbar_init(&m->odone, 1);
+    mbar_init(&m->drain, 1);
+    mbar_init(&m->sgrp, kSoftmaxThreads);
+    mbar_init(&m->pgrp, 128);
+    m->abort = 0;
     fence_mbar_init();
   }
-  // Q[t] -> shared memory, 8 swizzled K-major slabs of [128 heads x 64 dims].
-  const uint8_t* q_t = static_cast<const uint8_t*>(p.q) + (int64_t)t * p.H * (kLatent * 2);
-  for (int i = tid; i < kM * 64; i += kThreads) {
-    const int h = i >> 6, j = i & 63;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (h < p.H) v = __ldg(reinterpret_cast<const uint4*>(q_t + h * (kLatent * 2)) + j);
-    *reinterpret_cast<uint4*>(sQ + (j >> 3) * kQSlab + sw128_off(h, j & 7)) = v;
+  if (warp == 0) {
+    tmem_alloc(&m->tmem_base, kTmemCols);
+    tmem_relinquish();
   }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers exist before anyone arrives on them remotely
   tc_fence_after();
-  const uint32_t tmem = misc->tmem_base;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tmem = m->tmem_base;
 
-  const CacheView cv{p.cache, (int64_t)p.P * kRowBytes, (int64_t)p.P * kDataBytes, p.P};
-  const int32_t* gidx_t = p.gidx + (int64_t)t * N;
-  const int64_t n_slots = p.num_pages * p.P;
-  const float sl2 = p.scale * kLog2e;
-  constexpr uint32_t kIdescQK = idesc_bf16_f32(kM, kTileRows, false, false);
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(kM, kDHalf, false, true);
-  const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aP = smem_u32(sP);
-
-  float m_run = -INFINITY;  // running max, log2 domain
-  float l_run = 0.f;        // running denominator (without sink)
-  bool o_live = false;      // the O accumulator holds data
-  bool aborted = false;
-  uint32_t phase = 0;
-
-  for (int tile = tile_begin; tile < tile_end; ++tile) {
-    const int row0 = tile * kTileRows;
-    if (tid < kTileRows) {
-      const int r = row0 + tid;
-      int32_t g = r < N ? __ldg(gidx_t + r) : -1;
-      if ((int64_t)g >= n_slots) g = -1;
-      misc->slot[tid] = g;
-    }
-    __syncthreads();
-
-    // Gather + dequant: 64 rows x 36 sixteen-byte input chunks (28 NoPE, 8 RoPE).
-#pragma unroll 6
-    for (int i = tid; i < kTileRows * 36; i += kThreads) {
-      const int r = i / 36, j = i - (i / 36) * 36;
-      const int32_t g = misc->slot[r];
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (j < 28) {
-        if (g >= 0) {
-          const uint4 raw = ldg16<ALIGN16>(row_data(cv, g) + j * 16);
-          const float sc = ue8m0_to_float(__ldg(row_scales(cv, g) + (j >> 2)));
-          dequant16(raw, sc, lo, hi);
-        }
-        uint8_t* slab = sK + (j >> 2) * kKSlab;
-        *reinterpret_cast<uint4*>(slab + sw128_off(r, (j & 3) * 2)) = lo;
-        *reinterpret_cast<uint4*>(slab + sw128_off(r, (j & 3) * 2 + 1)) = hi;
-      } else {
-        if (g >= 0) lo = scrub_bf16x8(ldg16<ALIGN16>(row_data(cv, g) + kNope + (j - 28) * 16));
-        *reinterpret_cast<uint4*>(sK + 7 * kKSlab + sw128_off(r, j - 28)) = lo;
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // S = Q K^T : M=128, N=64, K=512 (32 UMMAs of K=16).
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 32; ++kk) {
-        const uint32_t slab = kk >> 2, koff = (kk & 3) * 32;
-        umma_ss(tmem + kColS, desc_sw128(aQ + slab * kQSlab + koff, 16, 1024),
-                desc_sw128(aK + slab * kKSlab + koff, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(&misc->mma_bar);
-    }
-    bool ok = mbar_wait_bounded(&misc->mma_bar, phase, kWaitLimitNs);
-    phase ^= 1u;
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    tc_fence_after();
-
-    // Online softmax for head row `tid` over the 64 columns of this tile.
-    uint32_t sraw[2][32];
-    tmem_ld32(tmem + lane_base + kColS, sraw[0]);
-    tmem_ld32(tmem + lane_base + kColS + 32, sraw[1]);
-    tmem_wait_ld();
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const float x = misc->slot[j] >= 0 ? __uint_as_float(sraw[j >> 5][j & 31]) * sl2 : -INFINITY;
-      sraw[j >> 5][j & 31] = __float_as_uint(x);
-      tmax = fmaxf(tmax, x);
-    }
-    const float m_new = fmaxf(m_run, tmax);
-    float alpha = 1.f, psum = 0.f;
-    uint32_t pk[32];
-    if (m_new == -INFINITY) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = 0u;
-    } else {
-      alpha = ex2(m_run - m_new);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float x0 = __uint_as_float(sraw[(2 * i) >> 5][(2 * i) & 31]);
-        const float x1 = __uint_as_float(sraw[(2 * i + 1) >> 5][(2 * i + 1) & 31]);
-        const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
-        psum += p0 + p1;  // the denominator keeps the unrounded weights
-        pk[i] = bf16x2_bits(__floats2bfloat162_rn(p0, p1));
-      }
-    }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      *reinterpret_cast<uint4*>(sP + sw128_off(tid, ch)) =
-          make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-    // Rescale the 256 accumulator columns when any lane of the warp needs it: tcgen05.ld/st
-    // are warp-collective, so the branch must be warp-uniform (lanes with alpha == 1
-    // rewrite their values unchanged).
-    const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
-    if (o_live && rescale) {
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax + UMMA issue
+    // Thread (h, hc): head h = TMEM lane h, column half hc of every 128-column tile.
+    const int h = tid & 127;
+    const int hc = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool issuer = tid == 0;
+    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTile, false, false);
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDHalf, false, true);
+    const uint32_t a_stage = smem_u32(smem);
+    bool ok = true;
+    uint32_t sgrp_phase = 0;  // uses of the softmax-group rendezvous so far (parity)
+    {  // this thread's half of head h's Q half -> TMEM columns [64 hc, 64 hc + 64) of lane h
+      const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
+                                                         ((int64_t)t * p.H + h) * (kLatent * 2) + half * (kDHalf * 2) +
+                                                         hc * 256);
 #pragma unroll 1
-      for (int cc = 0; cc < kDHalf / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tmem + lane_base + kColO + cc * 32, o);
-      }
-      tmem_wait_st();
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // O_half += P V_half : M=128, N=256, K=64 (4 UMMAs of K=16); V is the same tile,
-    // read MN-major (dims contiguous): 64-dim slabs 8 KB apart, 8-row groups 1 KB apart.
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        umma_ss(tmem + kColO, desc_sw128(aP + kk * 32, 16, 1024),
-                desc_sw128(aK + (4 * half) * kKSlab + kk * 2048, kKSlab, 1024), kIdescPV,
-                (o_live || kk > 0) ? 1u : 0u);
-      }
-      umma_commit(&misc->mma_bar);
-    }
-    ok = mbar_wait_bounded(&misc->mma_bar, phase, kWaitLimitNs);
-    phase ^= 1u;
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    tc_fence_after();
-    o_live = true;
-  }
-
-  if (aborted) {
-    // A bounded wait gave up: record it, give in-flight MMAs one more bounded chance to
-    // land, free TMEM and leave without writing outputs.
-    if (tid == 0 && p.status != nullptr) atomicOr(p.status, 1u);
-    mbar_wait_bounded(&misc->mma_bar, phase ^ 1u, kWaitLimitNs);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-      tc_fence_after();
-      tmem_dealloc(tmem, kTmemCols);
-    }
-    return;
-  }
-
-  // Epilogue: thread h finalises head h for this CTA's 256 output dims.
-  const int h = tid;
-  const bool head_ok = h < p.H;
-  if (p.S == 1) {
-    const float sink_nat = (p.sink != nullptr && head_ok) ? __ldg(p.sink + h) : -INFINITY;
-    const float ms = sink_nat * kLog2e;
-    const float M = fmaxf(m_run, ms);
-    float factor = 0.f, lse_v = -INFINITY;
-    if (M != -INFINITY) {
-      const float den = l_run * ex2(m_run - M) + (ms == -INFINITY ? 0.f : ex2(ms - M));
-      factor = ex2(m_run - M) / den;
-      // natural-log max taken from whichever term set it, so a sink-only row gives lse = sink exactly
-      lse_v = (M == m_run ? m_run * kLn2 : sink_nat) + log2f(den) * kLn2;
-    }
-    uint8_t* orow = static_cast<uint8_t*>(p.out) + ((int64_t)t * p.H + h) * (kLatent * 2) + half * (kDHalf * 2);
-#pragma unroll 1
-    for (int cc = 0; cc < kDHalf / 32; ++cc) {
-      uint32_t o[32];
-      if (o_live) {
-        tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
-        tmem_wait_ld();
-      }
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float a = o_live ? __uint_as_float(o[2 * i]) * factor : 0.f;
-        const float b = o_live ? __uint_as_float(o[2 * i + 1]) * factor : 0.f;
-        w[i] = bf16x2_bits(__floats2bfloat162_rn(a, b));
-      }
-      if (head_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-        dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-      }
-    }
-    if (head_ok && half == 0 && p.lse != nullptr) p.lse[(int64_t)t * p.H + h] = lse_v;
-  } else {
-    const float factor = l_run > 0.f ? 1.f / l_run : 0.f;
-    const int64_t prow = ((int64_t)t * p.S + split) * p.H + h;
-    float* orow = p.o_part + prow * kLatent + half * kDHalf;
-#pragma unroll 1
-    for (int cc = 0; cc < kDHalf / 32; ++cc) {
-      uint32_t o[32];
-      if (o_live) {
-        tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
-        tmem_wait_ld();
-      }
-      if (head_ok) {
-        float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          float4 v;
-          v.x = o_live ? __uint_as_float(o[4 * i + 0]) * factor : 0.f;
-          v.y = o_live ? __uint_as_float(o[4 * i + 1]) * factor : 0.f;
-          v.z = o_live ? __uint_as_float(o[4 * i + 2]) * factor : 0.f;
-          v.w = o_live ? __uint_as_float(o[4 * i + 3]) * factor : 0.f;
-          dst[i] = v;
+          const uint4 v = h < p.H ? __ldg(qrow + c2 * 8 + i) : make_uint4(0, 0, 0, 0);
+          r[4 * i] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
         }
+        tmem_st32(tmem + lane_base + kColQ + hc * 64 + c2 * 32, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&m->sgrp);
+      ok = wait_bar(&m->sgrp, sgrp_phase, m);
+      sgrp_phase ^= 1u;
+      tc_fence_after();
+    }
+    auto issue_qk = [&](int j) {  // S = Q K^T for tile j
+      const uint32_t base = a_stage + (j & 1) * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < kDHalf / 16; ++kk)
+        umma_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_sw128(base + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+                kIdescQK, kk > 0 ? 1u : 0u);
+      umma_commit(&m->sfull);
+    };
+    auto issue_pv = [&](int j) {  // O += P V for tile j, then free its stage
+      const uint32_t base = a_stage + (j & 1) * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        umma_ts(tmem + kColO, tmem + kColS + kk * 8, desc_sw128(base + kk * 2048, kSlab, 1024), kIdescPV,
+                (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&m->kempty[j & 1]);
+    };
+    if (ok && issuer && n > 0) {
+      if ((ok = wait_bar(&m->kfull[0], 0, m))) {
+        tc_fence_after();
+        issue_qk(0);
       }
     }
-    if (head_ok && half == 0) p.lse_part[prow] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    __syncwarp();
+
+    const uint32_t peer_xchg_row = mapa(smem_u32(xchg + h * 512), peer);
+    const uint32_t peer_xfull = mapa(smem_u32(&m->xfull), peer);
+    const uint32_t peer_xempty = mapa(smem_u32(&m->xempty), peer);
+    const uint8_t* my_xchg_row = xchg + h * 512;
+    const float sl2 = p.scale * kLog2e;
+    float m_ref = -INFINITY;  // reference max (log2 domain) the weights are taken against
+    float l_run = 0.f;        // this thread's share of the denominator relative to m_ref
+
+    for (int j = 0; j < n && ok; ++j) {
+      const int s = j & 1;
+      if (!(ok = wait_bar(&m->sfull, j & 1, m))) break;
+      tc_fence_after();
+      if (j > 0 && !(ok = wait_bar(&m->xempty, (j - 1) & 1, m, true))) break;
+      float x[64];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + kColS + hc * 64 + c2 * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t ch = hc * 16 + c2 * 8 + i;
+          st_cluster_v4(peer_xchg_row + ((ch ^ (h & 7)) << 4), r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c2 * 32 + i] = __uint_as_float(r[i]);
+      }
+      mbar_arrive_cluster(peer_xfull);
+      if (!(ok = wait_bar(&m->xfull, j & 1, m, true))) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t ch = hc * 16 + c;
+        const float4 v = *reinterpret_cast<const float4*>(my_xchg_row + ((ch ^ (h & 7)) << 4));
+        x[4 * c] += v.x;
+        x[4 * c + 1] += v.y;
+        x[4 * c + 2] += v.z;
+        x[4 * c + 3] += v.w;
+      }
+      mbar_arrive_cluster(peer_xempty);
+
+      const uint32_t mk0 = m->mask[s][2 * hc], mk1 = m->mask[s][2 * hc + 1];
+      float lmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const uint32_t bits = c < 32 ? mk0 : mk1;
+        const float v = ((bits >> (c & 31)) & 1u) ? x[c] * sl2 : -INFINITY;
+        x[c] = v;
+        lmax = fmaxf(lmax, v);
+      }
+      m->red_max[s][hc][h] = lmax;
+      // Both threads of head h have finished reading S (wait::ld above) before either
+      // overwrites its columns with P below.
+      tc_fence_before();
+      mbar_arrive(&m->sgrp);
+      if (!(ok = wait_bar(&m->sgrp, sgrp_phase, m))) break;
+      sgrp_phase ^= 1u;
+      tc_fence_after();
+      const float tmax = fmaxf(lmax, m->red_max[s][hc ^ 1][h]);
+      float alpha = 1.f;
+      const bool upd = tmax > m_ref + kRescaleThreshold;  // false while everything is masked
+      if (upd) {
+        alpha = ex2(m_ref - tmax);  // 0 when m_ref is -inf
+        m_ref = tmax;
+      }
+      float psum = 0.f;
+      uint32_t pk[32];
+      if (m_ref == -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(x[2 * i] - m_ref), p1 = ex2(x[2 * i + 1] - m_ref);
+          psum += p0 + p1;  // the denominator keeps the unrounded weights
+          pk[i] = bf16x2_bits(__floats2bfloat162_rn(p0, p1));
+        }
+      }
+      l_run = l_run * alpha + psum;
+      tmem_st32(tmem + lane_base + kColS + hc * 32, pk);
+      // PV of the previous tile finished before S of this one was committed, so O is idle.
+      if (j > 0 && __any_sync(0xffffffffu, upd)) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          const uint32_t col = kColO + hc * 128 + cc * 32;
+          tmem_ld32(tmem + lane_base + col, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + lane_base + col, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&m->pfull);
+      if (issuer) {
+        if ((ok = wait_bar(&m->pfull, j & 1, m))) {
+          tc_fence_after();
+          issue_pv(j);
+          if (j + 1 < n) {
+            if ((ok = wait_bar(&m->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1, m))) {
+              tc_fence_after();
+              issue_qk(j + 1);
+            }
+          } else {
+            umma_commit(&m->odone);
+          }
+        }
+      }
+      __syncwarp();
+      ok = ok && !aborted(m);
+    }
+    if (issuer && n == 0) mbar_arrive(&m->odone);
+    if (ok) ok = wait_bar(&m->odone, 0, m);
+    if (!ok) {
+      record_abort(m, p.status);
+      if (issuer) {
+        umma_commit(&m->drain);  // let issued UMMAs land before TMEM is freed
+        mbar_wait_bounded(&m->drain, 0, kWaitLimitNs);
+      }
+    } else {
+      // Epilogue: head h, local dims [128 hc, 128 hc + 128) of this CTA's 256.
+      m->red_sum[hc][h] = l_run;
+      mbar_arrive(&m->sgrp);
+      ok = wait_bar(&m->sgrp, sgrp_phase, m);
+      sgrp_phase ^= 1u;
+    }
+    if (!ok) {
+      record_abort(m, p.status);
+    } else {
+      const float l_tot = l_run + m->red_sum[hc ^ 1][h];
+      tc_fence_after();
+      const bool o_live = n > 0;
+      const bool head_ok = h < p.H;
+      const int d0 = half * kDHalf + hc * 128;  // first output dim of this thread
+      if (p.S == 1) {
+        const float sink_nat = (p.sink != nullptr && head_ok) ? __ldg(p.sink + h) : -INFINITY;
+        const float ms = sink_nat * kLog2e;
+        const float M = fmaxf(m_ref, ms);
+        float factor = 0.f, lse_v = -INFINITY;
+        if (M != -INFINITY) {
+          const float den = l_tot * ex2(m_ref - M) + (ms == -INFINITY ? 0.f : ex2(ms - M));
+          factor = ex2(m_ref - M) / den;
+          // natural-log max from whichever term set it, so a sink-only row gives lse = sink exactly
+          lse_v = (M == m_ref ? m_ref * kLn2 : sink_nat) + log2f(den) * kLn2;
+        }
+        uint8_t* orow = static_cast<uint8_t*>(p.out) + (((int64_t)t * p.H + h) * kLatent + d0) * 2;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          if (o_live) {
+            tmem_ld32(tmem + lane_base + kColO + hc * 128 + cc * 32, o);
+            tmem_wait_ld();
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = o_live ? __uint_as_float(o[2 * i]) * factor : 0.f;
+            const float b = o_live ? __uint_as_float(o[2 * i + 1]) * factor : 0.f;
+            w[i] = bf16x2_bits(__floats2bfloat162_rn(a, b));
+          }
+          if (head_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          }
+        }
+        if (head_ok && half == 0 && hc == 0 && p.lse != nullptr) p.lse[(int64_t)t * p.H + h] = lse_v;
+      } else {
+        const float factor = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        const int64_t prow = ((int64_t)t * p.S + split) * p.H + h;
+        float* orow = p.o_part + prow * kLatent + d0;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          if (o_live) {
+            tmem_ld32(tmem + lane_base + kColO + hc * 128 + cc * 32, o);
+            tmem_wait_ld();
+          }
+          if (head_ok) {
+            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 v;
+              v.x = o_live ? __uint_as_float(o[4 * i + 0]) * factor : 0.f;
+              v.y = o_live ? __uint_as_float(o[4 * i + 1]) * factor : 0.f;
+              v.z = o_live ? __uint_as_float(o[4 * i + 2]) * factor : 0.f;
+              v.w = o_live ? __uint_as_float(o[4 * i + 3]) * factor : 0.f;
+              dst[i] = v;
+            }
+          }
+        }
+        if (head_ok && half == 0 && hc == 0)
+          p.lse_part[prow] = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ gather + dequant
+    const int ptid = tid - kSoftmaxThreads;
+    const int pwarp = warp - 8;
+    const CacheView cv{p.cache, (int64_t)p.P * kRowBytes, (int64_t)p.P * kDataBytes, p.P};
+    const int32_t* gidx_t = p.gidx + (int64_t)t * N;
+    const int64_t n_slots = p.num_pages * p.P;
+    for (int j = 0; j < n; ++j) {
+      const int s = j & 1;
+      const int u = j >> 1;
+      if (u > 0 && !wait_bar(&m->kempty[s], (u - 1) & 1, m)) {
+        record_abort(m, p.status);
+        break;
+      }
+      const int row = (tile_begin + j) * kTile + ptid;
+      int32_t g = row < N ? __ldg(gidx_t + row) : -1;
+      if ((int64_t)g >= n_slots) g = -1;
+      m->slot[s][ptid] = g;
+      const uint32_t bits = __ballot_sync(0xffffffffu, g >= 0);
+      if (lane == 0) m->mask[s][pwarp] = bits;
+      mbar_arrive(&m->pgrp);
+      if (!wait_bar(&m->pgrp, j & 1, m)) {
+        record_abort(m, p.status);
+        break;
+      }
+      uint8_t* st = smem + s * kStageBytes;
+      if (half == 0)
+        fill_stage<0, ALIGN16>(st, m->slot[s], cv, ptid);
+      else
+        fill_stage<1, ALIGN16>(st, m->slot[s], cv, ptid);
+      fence_async_smem();
+      mbar_arrive(&m->kfull[s]);
+    }
   }
 
+  // Wind down: nobody may leave while the peer can still write into this CTA's shared
+  // memory, and TMEM is freed only after every tcgen05 access of this CTA is done.
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -334,18 +511,18 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   static bool attr_done[2][64] = {};
   if (dev < 64 && !attr_done[align16][dev]) {
-    e = align16 ? cudaFuncSetAttribute(attn_partial_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = align16 ? cudaFuncSetAttribute(attn_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes)
-                : cudaFuncSetAttribute(attn_partial_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                : cudaFuncSetAttribute(attn_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[align16][dev] = true;
   }
   const dim3 grid(2 * p.S, p.T);
   if (align16)
-    attn_partial_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+    attn_pair_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
   else
-    attn_partial_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
+    attn_pair_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 

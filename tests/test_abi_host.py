@@ -58,12 +58,12 @@ def test_split_selector_rules(lib):
     assert 8 <= s4 <= 32
     # large batch fills the GPU without splitting
     assert api.select_num_splits(_dims(T=256, H=64, K=512, W=128), 0, 152) == 1
-    # every split keeps at least one 64-row tile
+    # every split keeps at least one 128-row tile
     for T in (1, 2, 3, 5, 16):
         for N in (1, 63, 64, 65, 200, 640, 2176):
             d = _dims(T=T, K=N, W=0)
             s = api.select_num_splits(d, 0, 152)
-            tiles = -(-N // 64)
+            tiles = -(-N // 128)
             tps = -(-tiles // s)
             assert (s - 1) * tps < tiles
     # depends on shapes and SM count only (graph-safe): repeatable
