@@ -65,17 +65,15 @@ struct Misc {
   uint64_t odone;            // issuer commit -> softmax: every PV done
   uint64_t drain;            // UMMA self-drain before TMEM is freed after a failed wait
   uint64_t sgrp;             // softmax-group rendezvous (256 arrivals per use)
-  uint64_t pgrp;             // producer-group rendezvous (128 arrivals per use)
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t mask[kStages][4];        // valid-row bit masks of the staged tile
-  int32_t slot[kStages][kTile];     // converted slots of the staged tile
   float red_max[kStages][2][128];   // per-column-half tile maxima of each head
   float red_sum[2][128];            // per-column-half denominators at the end
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
-__device__ __forceinline__ float ex2(float x) { return exp2f(x); }
+__device__ __forceinline__ float ex2(float x) { return fast_exp2(x); }
 
 __device__ __forceinline__ bool aborted(const Misc* m) {
   return *reinterpret_cast<const volatile uint32_t*>(&m->abort) != 0u;
@@ -104,50 +102,90 @@ __device__ __forceinline__ uint32_t stage_off(uint32_t row, uint32_t d0) {
   return (d0 >> 6) * kSlab + sw128_off(row, (d0 & 63) >> 3);
 }
 
-// Gather + dequantise this CTA's half of 128 rows into stage `st`.  Half 0: NoPE bytes
-// [0,256) with scale codes 0..3.  Half 1: NoPE bytes [256,448) with codes 4..6, then the
-// 64 RoPE values.  Consecutive threads take consecutive 16-byte chunks of a row, so each
-// warp load instruction reads whole contiguous row segments; all loads are issued before
-// the first conversion so they overlap in flight.
-template <int HALF, bool ALIGN16>
-__device__ __forceinline__ void fill_stage(uint8_t* st, const int32_t* slots, const CacheView& cv, int ptid) {
-  constexpr int NC = HALF == 0 ? 16 : 20;  // 16-byte input chunks per row
+// Gather + dequantise this CTA's half of 128 rows.  Half 0: NoPE bytes [0,256) with scale
+// codes 0..3.  Half 1: NoPE bytes [256,448) with codes 4..6, then the 64 RoPE values.
+// Consecutive threads take consecutive 16-byte chunks of a row, so each warp load reads
+// whole contiguous row segments.  `issue` puts every load of the tile in flight (invalid
+// rows read slot 0 and are zeroed later); `store` converts and writes the swizzled stage.
+template <int HALF>
+struct Gather {
+  static constexpr int NC = HALF == 0 ? 16 : 20;  // 16-byte input chunks per row
   uint4 raw[NC];
   uint32_t code[NC];
+  int32_t slot[NC];
+
+  template <bool ALIGN16>
+  __device__ __forceinline__ void issue(const int32_t* gidx_tile, int rows_left, int64_t n_slots,
+                                        const CacheView& cv, int ptid) {
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    const int k = i * 128 + ptid;
-    const int row = k / NC, ch = k - (k / NC) * NC;
-    const int32_t g = slots[row];
-    raw[i] = make_uint4(0, 0, 0, 0);
-    code[i] = 0;
-    if (g >= 0) {
+    for (int i = 0; i < NC; ++i) {
+      const int row = (i * 128 + ptid) / NC;
+      int32_t g = row < rows_left ? ldg_nc_s32(gidx_tile + row) : -1;
+      slot[i] = ((int64_t)g >= n_slots) ? -1 : g;
+    }
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+      const int k = i * 128 + ptid;
+      const int ch = k - (k / NC) * NC;
+      const int32_t g = slot[i] >= 0 ? slot[i] : 0;
       const uint8_t* d = row_data(cv, g);
       if (HALF == 0) {
-        raw[i] = ldg16<ALIGN16>(d + ch * 16);
-        code[i] = __ldg(row_scales(cv, g) + (ch >> 2));
+        raw[i] = ldg16_early<ALIGN16>(d + ch * 16);
+        code[i] = ldg_nc_u8(row_scales(cv, g) + (ch >> 2));
       } else if (ch < 12) {
-        raw[i] = ldg16<ALIGN16>(d + 256 + ch * 16);
-        code[i] = __ldg(row_scales(cv, g) + 4 + (ch >> 2));
+        raw[i] = ldg16_early<ALIGN16>(d + 256 + ch * 16);
+        code[i] = ldg_nc_u8(row_scales(cv, g) + 4 + (ch >> 2));
       } else {
-        raw[i] = ldg16<ALIGN16>(d + kNope + (ch - 12) * 16);
+        raw[i] = ldg16_early<ALIGN16>(d + kNope + (ch - 12) * 16);
+        code[i] = 0;
       }
     }
   }
+
+  __device__ __forceinline__ void store(uint8_t* st, int ptid) const {
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    const int k = i * 128 + ptid;
-    const int row = k / NC, ch = k - (k / NC) * NC;
-    const bool valid = slots[row] >= 0;
-    if (HALF == 1 && ch >= 12) {
-      const uint4 v = valid ? scrub_bf16x8(raw[i]) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(st + stage_off(row, 192 + (ch - 12) * 8)) = v;
-    } else {
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (valid) dequant16(raw[i], ue8m0_to_float(code[i]), lo, hi);
-      *reinterpret_cast<uint4*>(st + stage_off(row, ch * 16)) = lo;
-      *reinterpret_cast<uint4*>(st + stage_off(row, ch * 16 + 8)) = hi;
+    for (int i = 0; i < NC; ++i) {
+      const int k = i * 128 + ptid;
+      const int row = k / NC, ch = k - (k / NC) * NC;
+      const bool valid = slot[i] >= 0;
+      if (HALF == 1 && ch >= 12) {
+        const uint4 v = valid ? scrub_bf16x8(raw[i]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(st + stage_off(row, 192 + (ch - 12) * 8)) = v;
+      } else {
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (valid) dequant16(raw[i], ue8m0_to_float(code[i]), lo, hi);
+        *reinterpret_cast<uint4*>(st + stage_off(row, ch * 16)) = lo;
+        *reinterpret_cast<uint4*>(st + stage_off(row, ch * 16 + 8)) = hi;
+      }
     }
+  }
+};
+
+// The producer role: for every tile, put the loads in flight, then wait for the stage to
+// be free, publish the tile's valid-row mask, convert, and signal the UMMA issuer.
+template <int HALF, bool ALIGN16>
+__device__ __forceinline__ void produce(uint8_t* smem, Misc* m, const AttnParams& p, const int32_t* gidx_t,
+                                        int tile_begin, int n, int ptid, int pwarp, int lane) {
+  const CacheView cv{p.cache, (int64_t)p.P * kRowBytes, (int64_t)p.P * kDataBytes, p.P};
+  const int64_t n_slots = p.num_pages * p.P;
+  Gather<HALF> gth;
+  for (int j = 0; j < n; ++j) {
+    const int s = j & 1;
+    const int u = j >> 1;
+    const int row0 = (tile_begin + j) * kTile;
+    const int rows_left = p.N - row0;
+    gth.template issue<ALIGN16>(gidx_t + row0, rows_left, n_slots, cv, ptid);
+    int32_t g = ptid < rows_left ? ldg_nc_s32(gidx_t + row0 + ptid) : -1;
+    if ((int64_t)g >= n_slots) g = -1;
+    if (u > 0 && !wait_bar(&m->kempty[s], (u - 1) & 1, m)) {
+      record_abort(m, p.status);
+      return;
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, g >= 0);
+    if (lane == 0) m->mask[s][pwarp] = bits;
+    gth.store(smem + s * kStageBytes, ptid);
+    fence_async_smem();
+    mbar_arrive(&m->kfull[s]);
   }
 }
 
@@ -183,7 +221,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
     mbar_init(&m->odone, 1);
     mbar_init(&m->drain, 1);
     mbar_init(&m->sgrp, kSoftmaxThreads);
-    mbar_init(&m->pgrp, 128);
     m->abort = 0;
     fence_mbar_init();
   }
@@ -458,36 +495,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
   } else {
     // ------------------------------------------------------------ gather + dequant
     const int ptid = tid - kSoftmaxThreads;
-    const int pwarp = warp - 8;
-    const CacheView cv{p.cache, (int64_t)p.P * kRowBytes, (int64_t)p.P * kDataBytes, p.P};
     const int32_t* gidx_t = p.gidx + (int64_t)t * N;
-    const int64_t n_slots = p.num_pages * p.P;
-    for (int j = 0; j < n; ++j) {
-      const int s = j & 1;
-      const int u = j >> 1;
-      if (u > 0 && !wait_bar(&m->kempty[s], (u - 1) & 1, m)) {
-        record_abort(m, p.status);
-        break;
-      }
-      const int row = (tile_begin + j) * kTile + ptid;
-      int32_t g = row < N ? __ldg(gidx_t + row) : -1;
-      if ((int64_t)g >= n_slots) g = -1;
-      m->slot[s][ptid] = g;
-      const uint32_t bits = __ballot_sync(0xffffffffu, g >= 0);
-      if (lane == 0) m->mask[s][pwarp] = bits;
-      mbar_arrive(&m->pgrp);
-      if (!wait_bar(&m->pgrp, j & 1, m)) {
-        record_abort(m, p.status);
-        break;
-      }
-      uint8_t* st = smem + s * kStageBytes;
-      if (half == 0)
-        fill_stage<0, ALIGN16>(st, m->slot[s], cv, ptid);
-      else
-        fill_stage<1, ALIGN16>(st, m->slot[s], cv, ptid);
-      fence_async_smem();
-      mbar_arrive(&m->kfull[s]);
-    }
+    if (half == 0)
+      produce<0, ALIGN16>(smem, m, p, gidx_t, tile_begin, n, ptid, warp - 8, lane);
+    else
+      produce<1, ALIGN16>(smem, m, p, gidx_t, tile_begin, n, ptid, warp - 8, lane);
   }
 
   // Wind down: nobody may leave while the peer can still write into this CTA's shared

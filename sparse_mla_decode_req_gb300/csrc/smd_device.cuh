@@ -98,6 +98,47 @@ __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
   }
 }
 
+// Loads through the read-only path as volatile PTX: the compiler keeps them in program
+// order and cannot sink them to their first use, so a batch of them is in flight at once.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u8(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ldg_nc_s32(const void* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+template <bool ALIGN16>
+__device__ __forceinline__ uint4 ldg16_early(const uint8_t* p) {
+  if constexpr (ALIGN16) {
+    return ldg_nc_v4(p);
+  } else {
+    const uint2 a = ldg_nc_v2(p), b = ldg_nc_v2(p + 8);
+    return make_uint4(a.x, a.y, b.x, b.y);
+  }
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22); -inf gives 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- misc PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
