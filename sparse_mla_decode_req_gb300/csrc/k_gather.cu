@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherParams p) {
   const int32_t slot = __ldg(p.gidx + row);
   uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
   if (slot >= 0 && (int64_t)slot < p.num_pages * p.P) {
-    CacheView c{p.cache, (int64_t)p.P * kRowBytes, (int64_t)p.P * kDataBytes, p.P};
+    const CacheView c = make_cache_view(p.cache, p.P);
     const uint8_t* data = row_data(c, slot);
     if (lane < 28) {
       const uint4 raw = ldg16<ALIGN16>(data + lane * 16);

@@ -26,16 +26,38 @@ struct CacheView {
   int64_t page_bytes;   // P * 584
   int64_t scale_start;  // P * 576: offset of the scale rows inside a page
   int32_t P;
+  int32_t log2P;        // log2(P) when P is a power of two, else -1
 };
 
+__host__ __device__ inline int32_t log2_if_pow2(int32_t P) {
+  if (P <= 0 || (P & (P - 1)) != 0) return -1;
+  int32_t l = 0;
+  while ((1 << l) < P) ++l;
+  return l;
+}
+
+__device__ __forceinline__ CacheView make_cache_view(const uint8_t* base, int32_t P) {
+  return CacheView{base, (int64_t)P * kRowBytes, (int64_t)P * kDataBytes, P, log2_if_pow2(P)};
+}
+
+// Page and in-page offset of a global slot (shifts for power-of-two page sizes).
+__device__ __forceinline__ void slot_page_off(const CacheView& c, int32_t slot, int32_t& page, int32_t& off) {
+  if (c.log2P >= 0) {
+    page = slot >> c.log2P;
+    off = slot & (c.P - 1);
+  } else {
+    page = slot / c.P;
+    off = slot - page * c.P;
+  }
+}
 __device__ __forceinline__ const uint8_t* row_data(const CacheView& c, int32_t slot) {
-  const int32_t page = slot / c.P;
-  const int32_t off = slot - page * c.P;
+  int32_t page, off;
+  slot_page_off(c, slot, page, off);
   return c.base + (int64_t)page * c.page_bytes + (int64_t)off * kDataBytes;
 }
 __device__ __forceinline__ const uint8_t* row_scales(const CacheView& c, int32_t slot) {
-  const int32_t page = slot / c.P;
-  const int32_t off = slot - page * c.P;
+  int32_t page, off;
+  slot_page_off(c, slot, page, off);
   return c.base + (int64_t)page * c.page_bytes + c.scale_start + (int64_t)off * kScaleBytes;
 }
 
@@ -47,34 +69,47 @@ __device__ __forceinline__ float ue8m0_to_float(uint32_t code) {
 
 // Zero every bf16 lane whose exponent field is all ones (inf or NaN).
 __device__ __forceinline__ uint32_t scrub_bf16x2(uint32_t v) {
-  const uint32_t bad = __vcmpeq2(v & 0x7F807F80u, 0x7F807F80u);
-  return v & ~bad;
+  const uint32_t t = v & 0x7F807F80u;
+  const uint32_t bad_lo = (t & 0xFFFFu) == 0x7F80u ? 0x0000FFFFu : 0u;
+  const uint32_t bad_hi = (t >> 16) == 0x7F80u ? 0xFFFF0000u : 0u;
+  return v & ~(bad_lo | bad_hi);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Magnitudes at or above this fp32 value round to infinity in bf16 (halfway between the
+// largest finite bf16, 0x1.fep127, and 2^128); NaN compares false.
+constexpr uint32_t kBf16OverflowBits = 0x7F7F8000u;
+
 // Two e4m3 bytes (low byte = lower element) times a power-of-two scale -> scrubbed bf16x2.
-// fp8 -> fp16 is exact for every e4m3 value; the fp32 product is exact unless it
-// overflows; the bf16 rounding is exact whenever the product stays in bf16's normal
-// range, so the result equals the exactly-rounded latent value.
-__device__ __forceinline__ uint32_t dequant_fp8x2(uint16_t two, float scale) {
-  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-  return scrub_bf16x2(bf16x2_bits(__floats2bfloat162_rn(f.x * scale, f.y * scale)));
+// fp8 -> fp16 is exact for every e4m3 value (hardware cvt, NaN stays NaN); the fp32
+// product is exact unless it overflows; the bf16 rounding is exact whenever the product
+// stays in bf16's normal range, so the result equals the exactly-rounded latent value.
+// Non-finite products and products that would round to infinity become 0.
+__device__ __forceinline__ uint32_t dequant_fp8x2(uint32_t two, float scale) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h2) : "r"(two));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  const float2 f = __half22float2(hv);
+  const float lim = __uint_as_float(kBf16OverflowBits);
+  float a = f.x * scale, b = f.y * scale;
+  a = fabsf(a) < lim ? a : 0.f;
+  b = fabsf(b) < lim ? b : 0.f;
+  return bf16x2_bits(__floats2bfloat162_rn(a, b));
 }
 
 // 16 fp8 bytes (uint4) -> 16 bf16 (two uint4), one scale for all.
 __device__ __forceinline__ void dequant16(const uint4 in, float scale, uint4& lo, uint4& hi) {
-  lo.x = dequant_fp8x2((uint16_t)(in.x & 0xFFFF), scale);
-  lo.y = dequant_fp8x2((uint16_t)(in.x >> 16), scale);
-  lo.z = dequant_fp8x2((uint16_t)(in.y & 0xFFFF), scale);
-  lo.w = dequant_fp8x2((uint16_t)(in.y >> 16), scale);
-  hi.x = dequant_fp8x2((uint16_t)(in.z & 0xFFFF), scale);
-  hi.y = dequant_fp8x2((uint16_t)(in.z >> 16), scale);
-  hi.z = dequant_fp8x2((uint16_t)(in.w & 0xFFFF), scale);
-  hi.w = dequant_fp8x2((uint16_t)(in.w >> 16), scale);
+  lo.x = dequant_fp8x2(in.x & 0xFFFFu, scale);
+  lo.y = dequant_fp8x2(in.x >> 16, scale);
+  lo.z = dequant_fp8x2(in.y & 0xFFFFu, scale);
+  lo.w = dequant_fp8x2(in.y >> 16, scale);
+  hi.x = dequant_fp8x2(in.z & 0xFFFFu, scale);
+  hi.y = dequant_fp8x2(in.z >> 16, scale);
+  hi.z = dequant_fp8x2(in.w & 0xFFFFu, scale);
+  hi.w = dequant_fp8x2(in.w >> 16, scale);
 }
 
 __device__ __forceinline__ uint4 scrub_bf16x8(uint4 v) {
@@ -157,14 +192,17 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase completes or
+// about 0.1 ms passes, instead of spinning on the issue slots its neighbours need.
+constexpr uint32_t kSuspendHintNs = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -206,10 +244,10 @@ __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
