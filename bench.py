@@ -247,12 +247,11 @@ def main(argv=None):
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = api._ptr
     conv_args = (ctypes.byref(dims), P(inp.block_table), P(inp.req_id), P(topk), P(swa), P(gidx), sp)
-    attn_dims = api.Dims(num_tokens=T, num_heads=H, num_requests=1, max_blocks_per_req=1,
-                         num_pages=inp.num_pages, block_size=w.block_size, topk=N, swa=0, pad_=0, bt_stride=1,
-                         topk_stride=max(N, 1), swa_stride=0)
+    attn_dims = api.attention_dims(T, H, N, inp.num_pages, w.block_size)
+    xchg = torch.empty(api.attention_xchg_size(attn_dims, w.max_splits, sms), dtype=torch.uint8, device=dev)
     attn_args = (ctypes.byref(attn_dims), P(inp.q), P(inp.kv_cache), P(gidx), P(inp.sink),
                  ctypes.c_float(inp.scale), int(w.max_splits), P(out), P(lse), P(o_part), P(lse_part),
-                 P(status), sp)
+                 P(status), P(xchg), ctypes.c_size_t(xchg.numel()), sp)
     comb_args = (T, S, H, P(o_part), P(lse_part), P(inp.sink), P(out), P(lse), sp)
 
     def step():
@@ -307,7 +306,7 @@ def main(argv=None):
     peaks, src = load_peaks()
     traffic = load_traffic(w.name)
     roof = roofline(H, rows_per_step, statistics.mean(attn_ms) / 1e3, peaks, src, traffic)
-    roof["kernel"] = "smd::attn_partial_kernel"
+    roof["kernel"] = "smd::attn_pair_kernel"
     roof["launch_ms_mean"] = statistics.mean(attn_ms)
 
     # end to end through the public call with host buffers: h2d of the step's inputs,

@@ -107,10 +107,20 @@ SMD_API int smd_select_num_splits(const smd_dims *dims, int num_splits, int num_
 /*
  * Device workspace bytes smd_sparse_mla_decode needs for the given split request
  * (same num_splits/num_sms meaning as smd_select_num_splits).  Holds a status word,
- * the converted indices [T, K+W] int32 and, when S > 1, the split partials
- * o_part f32 [T, S, H, 512] and lse_part f32 [T, S, H].  Returns 0 on bad dims.
+ * the converted indices [T, K+W] int32, when S > 1 the split partials o_part f32
+ * [T, S, H, 512] and lse_part f32 [T, S, H], and the attention kernel's exchange
+ * buffers (smd_attention_xchg_size).  Returns 0 on bad dims.
  */
 SMD_API size_t smd_workspace_size(const smd_dims *dims, int num_splits, int num_sms);
+
+/*
+ * Device bytes of the exchange buffers smd_sparse_mla_attention needs: the two CTAs that
+ * share a (token, split) work item each hold half of the 512 latent dims, and swap their
+ * partial QK scores of every 128-entry tile through these buffers (about 65 KB per CTA,
+ * one CTA pair per two SMs, at most min(T * S, num_sms / 2) pairs).  The content is
+ * scratch: nothing is read before the same call writes it.  Returns 0 on bad dims.
+ */
+SMD_API size_t smd_attention_xchg_size(const smd_dims *dims, int num_splits, int num_sms);
 
 /*
  * The whole decode step (conversion, fused gather + dequant + tcgen05 attention, and
@@ -146,13 +156,16 @@ SMD_API int smd_sparse_mla_decode(const smd_dims *dims, const void *q, const uin
  * S > 1: writes each split's normalised output o_part f32 [T, S, H, 512] and its
  * sink-free lse_part f32 [T, S, H] (-inf for a split without valid entries), to be
  * merged by smd_lse_combine; out/lse are not touched.  status (optional, device int32)
- * gets bit 0 set if a bounded wait inside the kernel gives up.  dims->topk + dims->swa is
- * the row length of gidx; the index pointers of dims are not used.
+ * gets bit 0 set if a bounded wait inside the kernel gives up (bit 1 if the kernel's
+ * shared memory was not 1024-byte aligned; nothing is computed then).  xchg: device
+ * scratch of xchg_bytes >= smd_attention_xchg_size(dims, num_splits, device SMs),
+ * 16-byte aligned (SMD_ERR_WORKSPACE if smaller).  dims->topk + dims->swa is the row
+ * length of gidx; the index pointers of dims are not used.
  */
 SMD_API int smd_sparse_mla_attention(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
                                      const int32_t *gidx, const float *sink, float scale, int num_splits,
                                      void *out, float *lse, float *o_part, float *lse_part,
-                                     int32_t *status, smd_stream_t stream);
+                                     int32_t *status, void *xchg, size_t xchg_bytes, smd_stream_t stream);
 
 /*
  * Step 1 alone: writes gidx i32 [T, K+W] (top-k entries first, window entries at

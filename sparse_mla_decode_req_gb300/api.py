@@ -60,8 +60,9 @@ _SIGS = {
     "smd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int]),
     "smd_sparse_mla_decode": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
                                              _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "smd_attention_xchg_size": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int]),
     "smd_sparse_mla_attention": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, ctypes.c_float, ctypes.c_int,
-                                                _P, _P, _P, _P, _P, _P]),
+                                                _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "smd_convert_req_index": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P]),
     "smd_gather_dequant": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, ctypes.c_int64, _P, _P]),
     "smd_lse_combine": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P]),
@@ -167,22 +168,36 @@ def sparse_mla_decode(q, kv_cache, block_table, req_id, topk_idx, swa_idx, sink,
     return out, lse
 
 
+def attention_xchg_size(dims: Dims, num_splits: int = 0, num_sms: int = 0) -> int:
+    n = load().smd_attention_xchg_size(ctypes.byref(dims), int(num_splits), int(num_sms))
+    if n == 0:
+        raise SmdError(SMD_ERR_INVALID_ARG, last_error())
+    return int(n)
+
+
+def attention_dims(T: int, H: int, N: int, num_pages: int, block_size: int = 64) -> Dims:
+    """smd_dims for the attention-only call over converted slots [T, N]."""
+    return Dims(num_tokens=T, num_heads=H, num_requests=1, max_blocks_per_req=1, num_pages=int(num_pages),
+                block_size=int(block_size), topk=N, swa=0, pad_=0, bt_stride=1, topk_stride=max(N, 1), swa_stride=0)
+
+
 def sparse_mla_attention(q, kv_cache, gidx, sink, scale: float, num_pages: int | None = None, num_splits: int = 0,
                          out=None, lse=None, o_part=None, lse_part=None, status=None, block_size: int = 64,
-                         stream=None):
+                         stream=None, xchg=None):
     """Fused gather + dequant + attention over converted slots gidx int32 [T, N].
 
     One split: returns (out, lse).  Several splits: returns (o_part, lse_part), the
-    per-split partials for ``lse_combine``.
+    per-split partials for ``lse_combine``.  ``xchg`` is the kernel's exchange scratch
+    (allocated here when not given).
     """
     T, N = int(gidx.shape[0]), int(gidx.shape[1])
     H = int(q.shape[1])
-    dims = Dims(num_tokens=T, num_heads=H, num_requests=1, max_blocks_per_req=1,
-                num_pages=int(kv_cache.shape[0] if num_pages is None else num_pages),
-                block_size=int(block_size), topk=N, swa=0, pad_=0, bt_stride=1, topk_stride=max(N, 1),
-                swa_stride=0)
-    S = select_num_splits(dims, num_splits, torch.cuda.get_device_properties(q.device).multi_processor_count)
+    dims = attention_dims(T, H, N, int(kv_cache.shape[0] if num_pages is None else num_pages), block_size)
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+    S = select_num_splits(dims, num_splits, sms)
     dev = q.device
+    if xchg is None:
+        xchg = torch.empty(attention_xchg_size(dims, num_splits, sms), dtype=torch.uint8, device=dev)
     if S == 1 and out is None:
         out = torch.empty(T, H, LATENT_DIM, dtype=torch.bfloat16, device=dev)
     if S == 1 and lse is None:
@@ -194,7 +209,8 @@ def sparse_mla_attention(q, kv_cache, gidx, sink, scale: float, num_pages: int |
     assert gidx.dtype == torch.int32 and gidx.is_contiguous()
     _check(load().smd_sparse_mla_attention(ctypes.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(gidx), _ptr(sink),
                                            ctypes.c_float(scale), int(num_splits), _ptr(out), _ptr(lse),
-                                           _ptr(o_part), _ptr(lse_part), _ptr(status), _stream(stream)))
+                                           _ptr(o_part), _ptr(lse_part), _ptr(status), _ptr(xchg),
+                                           ctypes.c_size_t(xchg.numel() * xchg.element_size()), _stream(stream)))
     return (out, lse) if S == 1 else (o_part, lse_part)
 
 

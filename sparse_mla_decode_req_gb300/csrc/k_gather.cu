@@ -25,8 +25,7 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherParams p) {
     const uint8_t* data = row_data(c, slot);
     if (lane < 28) {
       const uint4 raw = ldg16<ALIGN16>(data + lane * 16);
-      const float sc = ue8m0_to_float(__ldg(row_scales(c, slot) + (lane >> 2)));
-      dequant16(raw, sc, lo, hi);
+      dequant16_fast(raw, __ldg(row_scales(c, slot) + (lane >> 2)), lo, hi);
     } else {
       lo = scrub_bf16x8(ldg16<ALIGN16>(data + kNope + (lane - 28) * 32));
       hi = scrub_bf16x8(ldg16<ALIGN16>(data + kNope + (lane - 28) * 32 + 16));

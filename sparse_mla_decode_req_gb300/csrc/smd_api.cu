@@ -98,12 +98,17 @@ int select_splits(const smd_dims* d, int request, int sms) {
 }
 
 struct Layout {
-  size_t status = 0, gidx = 0, o_part = 0, lse_part = 0, total = 0;
+  size_t status = 0, gidx = 0, o_part = 0, lse_part = 0, xchg = 0, total = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-Layout workspace_layout(const smd_dims* d, int S) {
+// Exchange-buffer bytes of the attention launch for T tokens in S splits on `sms` SMs.
+size_t xchg_need(const smd_dims* d, int S, int sms) {
+  return smd::attn_xchg_bytes(smd::attn_pairs((int64_t)d->num_tokens * S, sms));
+}
+
+Layout workspace_layout(const smd_dims* d, int S, int sms) {
   Layout L;
   const size_t T = (size_t)d->num_tokens, N = (size_t)d->topk + (size_t)d->swa, H = (size_t)d->num_heads;
   size_t off = 0;
@@ -117,6 +122,8 @@ Layout workspace_layout(const smd_dims* d, int S) {
     L.lse_part = off;
     off += up256(T * (size_t)S * H * sizeof(float));
   }
+  L.xchg = off;
+  off += up256(xchg_need(d, S, sms));
   L.total = off;
   return L;
 }
@@ -183,7 +190,13 @@ SMD_API int smd_select_num_splits(const smd_dims* dims, int num_splits, int num_
 SMD_API size_t smd_workspace_size(const smd_dims* dims, int num_splits, int num_sms) {
   const int S = smd_select_num_splits(dims, num_splits, num_sms);
   if (S < 1) return 0;
-  return workspace_layout(dims, S).total;
+  return workspace_layout(dims, S, device_sms(num_sms)).total;
+}
+
+SMD_API size_t smd_attention_xchg_size(const smd_dims* dims, int num_splits, int num_sms) {
+  const int S = smd_select_num_splits(dims, num_splits, num_sms);
+  if (S < 1) return 0;
+  return xchg_need(dims, S, device_sms(num_sms));
 }
 
 SMD_API int smd_convert_req_index(const smd_dims* dims, const int32_t* block_table, const int32_t* req_id,
@@ -251,7 +264,7 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   const int sms = device_sms(0);
   if (sms <= 0) return fail(SMD_ERR_CUDA, "cannot query the device SM count");
   const int S = select_splits(dims, num_splits, sms);
-  const Layout L = workspace_layout(dims, S);
+  const Layout L = workspace_layout(dims, S, sms);
   if (workspace_bytes < L.total)
     return fail(SMD_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -275,6 +288,7 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   a.o_part = S > 1 ? reinterpret_cast<float*>(ws + L.o_part) : nullptr;
   a.lse_part = S > 1 ? reinterpret_cast<float*>(ws + L.lse_part) : nullptr;
   a.status = status;
+  a.xchg = ws + L.xchg;
   a.scale = scale;
   a.num_pages = dims->num_pages;
   a.T = dims->num_tokens;
@@ -284,6 +298,7 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   a.S = S;
   a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
   if (a.tiles_per_split < 1) a.tiles_per_split = 1;
+  a.G = smd::attn_pairs((int64_t)a.T * S, sms);
   e = smd::launch_attn(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (S > 1) {
@@ -297,7 +312,7 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
 SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
                                      const int32_t* gidx, const float* sink, float scale, int num_splits,
                                      void* out, float* lse, float* o_part, float* lse_part, int32_t* status,
-                                     smd_stream_t stream) {
+                                     void* xchg, size_t xchg_bytes, smd_stream_t stream) {
   g_err[0] = '\0';
   const int rc = check_dims(dims);
   if (rc != SMD_OK) return rc;
@@ -315,6 +330,9 @@ SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const 
   if (!aligned16(q) || !aligned16(kv_cache) || (out != nullptr && !aligned16(out)) ||
       (o_part != nullptr && !aligned16(o_part)))
     return fail(SMD_ERR_INVALID_ARG, "q/kv_cache/out/o_part not 16-byte aligned");
+  const size_t xneed = xchg_need(dims, S, sms);
+  if (xchg == nullptr || !aligned16(xchg)) return fail(SMD_ERR_INVALID_ARG, "xchg is NULL or not 16-byte aligned");
+  if (xchg_bytes < xneed) return fail(SMD_ERR_WORKSPACE, "xchg %zu bytes < required %zu", xchg_bytes, xneed);
   const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
   smd::AttnParams a{};
   a.q = q;
@@ -326,6 +344,7 @@ SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const 
   a.o_part = S > 1 ? o_part : nullptr;
   a.lse_part = S > 1 ? lse_part : nullptr;
   a.status = reinterpret_cast<uint32_t*>(status);
+  a.xchg = static_cast<uint8_t*>(xchg);
   a.scale = scale;
   a.num_pages = dims->num_pages;
   a.T = dims->num_tokens;
@@ -335,6 +354,7 @@ SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const 
   a.S = S;
   a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
   if (a.tiles_per_split < 1) a.tiles_per_split = 1;
+  a.G = smd::attn_pairs((int64_t)a.T * S, sms);
   const cudaError_t e = smd::launch_attn(a, stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "attention launch");
 }

@@ -50,13 +50,19 @@ struct AttnParams {
   float* o_part;          // [T, S, H, 512]            (S > 1)
   float* lse_part;        // [T, S, H]                 (S > 1)
   uint32_t* status;       // device status word
+  uint8_t* xchg;          // partial-score exchange buffers, attn_xchg_bytes(G) bytes
   float scale;
   int64_t num_pages;
   int32_t T, H, N, P, S;
   int32_t tiles_per_split;
+  int32_t G;              // CTA pairs launched; pair c takes work items c, c + G, ...
 };
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
 int attn_ctas_per_split();
+// CTA pairs the attention kernel launches for `items` (token, split) work items on a
+// device with `sms` SMs, and the exchange-buffer bytes that many pairs need.
+int attn_pairs(int64_t items, int sms);
+size_t attn_xchg_bytes(int pairs);
 
 // Sets the thread-local message returned by smd_last_error() and returns `code`.
 int set_error(int code, const char* fmt, ...);

@@ -70,15 +70,27 @@ def test_split_selector_rules(lib):
     assert api.select_num_splits(_dims(), 0, 152) == api.select_num_splits(_dims(), 0, 152)
 
 
+XCHG_PER_CTA = 16 * 256 * 16 + 256 * 4   # 16 pieces x 256 softmax threads x 16 B, then one scale each
+
+
+def _xchg(items, sms):
+    pairs = min(items, sms // 2) if items > 0 else 1
+    return pairs * 2 * XCHG_PER_CTA
+
+
 def test_workspace_size_layout(lib):
     d = _dims(T=4, H=128, K=2048, W=128)
     s = api.select_num_splits(d, -8, 152)
     n = api.workspace_size(d, -8, 152)
     T, N, H = 4, 2176, 128
-    need = 256 + T * N * 4 + T * s * H * 512 * 4 + T * s * H * 4
-    assert need <= n <= need + 3 * 256
+    need = 256 + T * N * 4 + T * s * H * 512 * 4 + T * s * H * 4 + _xchg(T * s, 152)
+    assert need <= n <= need + 4 * 256
+    assert api.attention_xchg_size(d, -8, 152) == _xchg(T * s, 152)
     d1 = _dims(T=256, H=64, K=512, W=128)
-    assert api.workspace_size(d1, 1, 152) == 256 + ((256 * 640 * 4 + 255) // 256) * 256
+    up = lambda x: (x + 255) // 256 * 256
+    assert api.workspace_size(d1, 1, 152) == 256 + up(256 * 640 * 4) + up(_xchg(256, 152))
+    # the exchange scratch is bounded by the SM count, not by the batch
+    assert api.attention_xchg_size(d1, 1, 152) == api.attention_xchg_size(_dims(T=4096, H=64, K=512, W=128), 1, 152)
 
 
 @pytest.mark.parametrize("field,value", [("num_heads", 0), ("num_heads", 129), ("block_size", 0),
