@@ -47,6 +47,8 @@
 // thread 0 also issues the UMMAs and warp 0 owns the TMEM allocation), warps 8-15
 // gather/dequant.  Every wait is bounded; a wait that gives up records bit 0 in the
 // status word and the CTA winds down (draining its UMMAs, freeing TMEM).
+#include <cuda.h>
+
 #include "smd_device.cuh"
 #include "smd_internal.h"
 
@@ -60,8 +62,9 @@ constexpr int kGroupThreads = 128;          // one producer group = 4 warps
 constexpr int kThreads = kSoftmaxThreads + 2 * kGroupThreads;
 constexpr uint32_t kSoftmaxRegs = 168, kProducerRegs = 88;
 static_assert(kSoftmaxThreads * kSoftmaxRegs + 2 * kGroupThreads * kProducerRegs == 65536, "register split");
-constexpr int kChunkRows = 32;
-constexpr int kRingSlots = 3;               // raw chunk slots per producer group
+constexpr int kProducerThreads = 2 * kGroupThreads;  // warps 8-15
+constexpr int kChunkRows = 64;              // rows per raw chunk (two per tile)
+constexpr int kRingSlots = 3;               // raw chunk slots
 constexpr uint32_t kSlab = kTile * 128;     // [128 rows x 64 dims] bf16 = 16 KB
 constexpr uint32_t kStageBytes = 4 * kSlab; // 64 KB
 constexpr uint32_t kOffP = 2 * kStageBytes;              // P: 2 slabs [128 heads x 64 rows]
@@ -75,19 +78,20 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between resca
 constexpr float kQMax = 32767.f;           // int16 range of the exchanged partials
 constexpr float kFixedMax = 64.f;          // largest |partial| (log2 units) sent as int16
 
-// Raw ring row format of each half: the half's data bytes, then the 8-byte scale row,
-// padded to a multiple of 16 bytes so that consecutive rows start 4 banks apart.
+// A raw chunk of one half: 64 rows of the half's data bytes (as the TMA gathers write
+// them, back to back), then the 64 rows' 8-byte scale rows.
 template <int HALF>
 struct RawFmt {
   static constexpr int NN = HALF == 0 ? 16 : 12;     // NoPE 16-byte pieces per row
   static constexpr int NR = HALF == 0 ? 0 : 8;       // RoPE pieces per row
   static constexpr int NP = NN + NR;
-  static constexpr int STRIDE = NP * 16 + 16;        // 272 / 336
-  static constexpr int CHUNK = kChunkRows * STRIDE;  // 8704 / 10752
+  static constexpr int DATA = NP * 16;               // 256 / 320 bytes of a row
+  static constexpr int SCALES = kChunkRows * DATA;   // offset of the scale rows
+  static constexpr int SLOT = SCALES + kChunkRows * 8;
   static constexpr int BYTE0 = HALF == 0 ? 0 : 256;  // first row byte of the half
   static constexpr int CODE0 = HALF == 0 ? 0 : 4;    // first scale code of the half
 };
-constexpr uint32_t kRingBytes = 2 * kRingSlots * RawFmt<1>::CHUNK;
+constexpr uint32_t kRingBytes = kRingSlots * RawFmt<1>::SLOT;
 constexpr uint32_t kOffMisc = kOffRing + kRingBytes;
 
 // Exchange buffer of one CTA (what its peer writes into): 16 pieces x 256 threads x 16 B
@@ -96,32 +100,34 @@ constexpr uint32_t kXchgData = 16u * kSoftmaxThreads * 16u;
 constexpr uint32_t kXchgRegion = kXchgData + kSoftmaxThreads * 4u;
 
 struct Misc {
-  uint64_t kfull[2];         // producer group g -> issuer: stage g filled (128 arrivals)
-  uint64_t kempty[2];        // PV commit -> producer group: stage consumed
+  uint64_t kfull[2];         // producers -> issuer: stage filled (224 converter arrivals)
+  uint64_t kempty[2];        // PV commit -> producers: stage consumed
   uint64_t sfull;            // QK commit -> softmax: S partial ready
   uint64_t sfree;            // softmax -> issuer: S loaded into registers (256 arrivals)
   uint64_t pfull;            // softmax -> issuer: P in shared memory, O rescaled (256 arrivals)
   uint64_t pvdone;           // PV commit -> softmax: P buffer and O free again
   uint64_t xfull;            // peer softmax -> softmax: peer partial written (256 remote arrivals)
-  uint64_t xempty;           // peer softmax -> softmax: peer read our last partial (256 remote)
+  uint64_t xempty;           // peer softmax -> softmax: the peer's P slices are free (256 remote)
   uint64_t odone;            // last PV commit of an item -> softmax: O final
   uint64_t drain;            // issuer self-drain before TMEM is freed after a failed wait
   uint64_t sgrp;             // softmax-group rendezvous (256 arrivals per use)
-  uint64_t rawfull[2][kRingSlots];  // cp.async completion of a raw chunk (128 arrivals)
+  uint64_t qready;           // softmax -> issuer: an item's Q is in TMEM (256 arrivals)
+  uint64_t rawfull[kRingSlots];   // raw chunk landed (loader expect-tx + 32 scale-copy arrivals)
+  uint64_t rawempty[kRingSlots];  // raw chunk converted (224 converter arrivals)
   uint64_t hpair[4];         // warps w and w+4 (the two threads of heads 32w..32w+31): 64
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t mask[2][4];              // valid-row bit masks of each stage's four chunks
-  uint32_t maskring[2][kRingSlots]; // valid-row mask of each raw chunk
-  int32_t gbuf[2][kTile];           // converted slots of each group's next tile
+  uint32_t mask[2][4];              // valid-row bit masks of each stage's 32-row quarters
+  uint32_t maskring[kRingSlots][2]; // valid-row masks of each raw chunk
   float red[2][2][128];             // per-column-half tile maxima, then final denominators
+  float xscale[kSoftmaxThreads];    // scale of each thread's received partials (< 0: fp32 in L2)
 };
 // The stages need 1024-byte alignment; dynamic shared memory starts 1024-aligned here
 // (checked at run time), so no slack is reserved.
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-__device__ __align__(16) uint8_t g_zero_row[16];  // source of the copies of masked rows
+__device__ __align__(16) uint8_t g_zero_row[320];  // source of the copies of masked rows
 
 __device__ __forceinline__ float ex2(float x) { return fast_exp2(x); }
 
@@ -167,17 +173,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ float ld_global_cg_f32(const void* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
 }
 
 // int16 fixed-point codec without conversion instructions.  Encode: adding 1.5 * 2^23
@@ -242,166 +246,386 @@ struct TileCursor {
   }
 };
 
-// A 16-byte piece of a cache row into shared memory: one copy when the row is 16-byte
-// aligned, two 8-byte copies otherwise (pages of an odd slot count).
-template <bool ALIGN16>
-__device__ __forceinline__ void cp_piece(uint32_t dst, const uint8_t* src) {
-  if constexpr (ALIGN16) {
-    cp_async16(dst, src);
-  } else {
-    cp_async8(dst, src);
-    cp_async8(dst + 8, src + 8);
-  }
+// TMA gather of four rows of the cache viewed as a 2-D tensor of 16-byte-spaced rows
+// (row y = bytes [16y, 16y + 576), u16 elements): rows y0..y3, elements [x, x + box),
+// written back to back at `dst`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2,
+                                            int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
 }
 
-// The producer role of group `g` (128 threads, gt = 0..127) for this CTA's half.
-template <int HALF, bool ALIGN16>
-__device__ __forceinline__ void produce(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int items, int g,
-                                        int gt) {
+// Walks the 64-row chunks (two per tile) of the CTA's tile sequence.
+struct ChunkCursor {
+  TileCursor t;
+  int c;  // chunk of the tile
+  __device__ void init(const AttnParams& p, int w0, int G, int items) {
+    t.init(p, w0, G, items);
+    c = 0;
+  }
+  __device__ bool valid() const { return t.valid(); }
+  __device__ void next(const AttnParams& p) {
+    if (c == 0) {
+      c = 1;
+    } else {
+      c = 0;
+      t.next(p);
+    }
+  }
+  // gidx offset of the chunk's first row and the rows it has inside the entry list
+  __device__ int64_t row0() const { return t.row0 + c * kChunkRows; }
+  __device__ int rows() const { return t.rows - c * kChunkRows; }
+};
+
+// Dequantises the 16-byte NoPE piece `k` of a raw row (scale code from its scale row)
+// into the stage, or zeros when the row is masked.
+// (elements in the (d0, d2, d1, d3) order of dequant16_perm_*; `fast` must be warp-uniform
+// and true only when no piece of the warp holds a NaN byte or a code above 134).
+template <bool FAST>
+__device__ __forceinline__ void convert_nope(uint8_t* stage, int srow, int k, uint4 raw, uint32_t code, bool valid) {
+  uint4 lo, hi;
+  if (!valid) {
+    raw = make_uint4(0, 0, 0, 0);
+    code = 0;
+  }
+  if constexpr (FAST)
+    dequant16_perm_fast(raw, code, lo, hi);
+  else
+    dequant16_perm_exact(raw, code, lo, hi);
+  *reinterpret_cast<uint4*>(stage + stage_off(srow, k * 16)) = lo;
+  *reinterpret_cast<uint4*>(stage + stage_off(srow, k * 16 + 8)) = hi;
+}
+
+// The control warp (warp 8): a non-blocking event loop that (TMA mode) puts the raw
+// chunks in flight, four rows per TMA gather, running as far ahead as the 3-slot ring
+// allows, and issues every UMMA of the CTA from lane 0: QK of a tile once its stage is
+// filled and S is free (or, for an item's first tile, once the item's Q is in TMEM), PV
+// of a tile once its P is in shared memory.  Keeping the issue off the softmax warps
+// keeps them in step with each other.
+constexpr int kConverters = kProducerThreads - 32;
+
+template <int HALF, bool TMA>
+__device__ __forceinline__ void control_warp(uint8_t* smem, Misc* m, const AttnParams& p, const CUtensorMap* map,
+                                             int cid, int items, uint32_t tmem, int lane) {
   using F = RawFmt<HALF>;
   const CacheView cv = make_cache_view(p.cache, p.P);
   const int64_t n_slots = p.num_pages * p.P;
-  const int gw = gt >> 5, lane = gt & 31;
-  const uint32_t bar_id = 1 + g;
-  uint8_t* ring = smem + kOffRing + g * kRingSlots * F::CHUNK;
-  uint8_t* stage = smem + g * kStageBytes;
-
-  // Tiles of this group: the CTA's tiles g, g+2, g+4, ...
-  TileCursor conv, iss, pre;
-  conv.init(p, cid, p.G, items);
-  if (g == 1 && conv.valid()) conv.next(p);
-  iss = conv;
-  pre = conv;
-  auto skip2 = [&](TileCursor& c) {
-    if (c.valid()) c.next(p);
-    if (c.valid()) c.next(p);
+  uint8_t* ring = smem + kOffRing;
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTile, false, false);
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDHalf, false, true);
+  const uint32_t a_stage = smem_u32(smem);
+  const uint32_t a_p = smem_u32(smem + kOffP);
+  auto issue_qk = [&](int jj) {  // S = Q K^T for tile jj
+    const uint32_t base = a_stage + (jj & 1) * kStageBytes;
+#pragma unroll
+    for (int kk = 0; kk < kDHalf / 16; ++kk)
+      umma_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_sw128(base + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+              kIdescQK, kk > 0 ? 1u : 0u);
+    umma_commit(&m->sfull);
   };
-  auto load_gidx = [&](const TileCursor& c) -> int32_t {
-    if (!c.valid() || gt >= c.rows) return -1;
-    const int32_t v = ldg_nc_s32(p.gidx + c.row0 + gt);
+  auto issue_pv = [&](int jj, bool first) {  // O += P V for tile jj, then free its stage and P
+    const uint32_t base = a_stage + (jj & 1) * kStageBytes;
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      umma_ss(tmem + kColO, desc_sw128(a_p + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+              desc_sw128(base + kk * 2048, kSlab, 1024), kIdescPV, (!first || kk > 0) ? 1u : 0u);
+    umma_commit(&m->kempty[jj & 1]);
+    umma_commit(&m->pvdone);
+  };
+  auto load_gidx = [&](const ChunkCursor& c, int r) -> int32_t {
+    if (!c.valid() || r >= c.rows()) return -1;
+    const int32_t v = ldg_nc_s32(p.gidx + c.row0() + r);
     return ((int64_t)v >= n_slots) ? -1 : v;
   };
-  if (!conv.valid()) return;
-
-  // Prologue: this tile's slots into gbuf, the next tile's in a register.
-  m->gbuf[g][gt] = load_gidx(conv);
-  skip2(pre);
-  int32_t gpre = load_gidx(pre);
-  named_bar_sync(bar_id, kGroupThreads);
-
-  int iss_chunk = 0;  // chunk of `iss` the next issue copies
-  int q_issue = 0;    // group-local chunk sequence number of the next issue
-  auto issue = [&]() {
-    const int slot = q_issue % kRingSlots;
-    const uint32_t dst = smem_u32(ring + slot * F::CHUNK);
-    const int32_t* gb = m->gbuf[g] + iss_chunk * kChunkRows;
-    auto src_row = [&](int r, const uint8_t*& d, const uint8_t*& sc) {
-      const int32_t s = gb[r];
-      d = g_zero_row;
-      sc = g_zero_row;
-      if (s >= 0) {
-        int32_t page, off;
-        slot_page_off(cv, s, page, off);
-        const uint8_t* pg = cv.base + (int64_t)page * cv.page_bytes;
-        d = pg + (int64_t)off * kDataBytes + F::BYTE0;
-        sc = pg + cv.scale_start + (int64_t)off * kScaleBytes;
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // pieces 0..15: half a warp per 256-byte row segment
-      const int r = gw * 8 + 2 * i + (lane >> 4), k = lane & 15;
-      const uint8_t *d, *sc;
-      src_row(r, d, sc);
-      cp_piece<ALIGN16>(dst + r * F::STRIDE + k * 16, d == g_zero_row ? d : d + k * 16);
-    }
-    if (F::NP > 16) {  // pieces 16..19 of the second half: a quarter warp per row
-      const int r = gw * 8 + (lane >> 2), k = 16 + (lane & 3);
-      const uint8_t *d, *sc;
-      src_row(r, d, sc);
-      cp_piece<ALIGN16>(dst + r * F::STRIDE + k * 16, d == g_zero_row ? d : d + k * 16);
-    }
-    if (gw == 0) {  // scale rows, and the chunk's valid-row mask
-      const uint8_t *d, *sc;
-      src_row(lane, d, sc);
-      cp_async8(dst + lane * F::STRIDE + F::NP * 16, sc);
-      const uint32_t bits = __ballot_sync(0xffffffffu, gb[lane] >= 0);
-      if (lane == 0) m->maskring[g][slot] = bits;
-    }
-    cp_async_arrive(&m->rawfull[g][slot]);
-    ++q_issue;
-    if (++iss_chunk == kTile / kChunkRows) {
-      iss_chunk = 0;
-      skip2(iss);
-    }
+  const int32_t rows_per_page16 = p.P * (kRowBytes / 8) / 2;  // P * 584 / 16 (TMA mode: P even)
+  auto row16 = [&](int32_t sl) -> int32_t {  // 16-byte row index of slot sl's data row
+    int32_t page, off;
+    slot_page_off(cv, sl, page, off);
+    return page * rows_per_page16 + off * (kDataBytes / 16);
+  };
+  auto scale_row = [&](int32_t sl) -> const uint8_t* {
+    if (sl < 0) return g_zero_row;
+    int32_t page, off;
+    slot_page_off(cv, sl, page, off);
+    return cv.base + (int64_t)page * cv.page_bytes + cv.scale_start + (int64_t)off * kScaleBytes;
   };
 
-  // Up to kRingSlots chunks in flight (they all belong to the first tile).
-  for (int i = 0; i < kRingSlots && iss.valid(); ++i) issue();
+  // chunk issue state (TMA mode): slots of rows lane and lane + 32 of the next two chunks
+  ChunkCursor iss, pre;
+  iss.init(p, cid, p.G, items);
+  pre = iss;
+  int32_t ga0 = -1, gb0 = -1, ga1 = -1, gb1 = -1;
+  if (TMA) {
+    ga0 = load_gidx(pre, lane);
+    gb0 = load_gidx(pre, lane + 32);
+    pre.next(p);
+    ga1 = load_gidx(pre, lane);
+    gb1 = load_gidx(pre, lane + 32);
+  }
+  int q_issue = 0;
+  // MMA issue state
+  TileCursor qkc, pvc;
+  qkc.init(p, cid, p.G, items);
+  pvc = qkc;
+  int jq = 0, jp = 0;  // tile sequence numbers of the next QK and PV
+  int neq = 0;         // index (among items with tiles) of qkc's item
+  uint64_t idle_since = 0;
 
-  const int cr = gt >> 2, cs = gt & 3;  // converter: row of the chunk, quarter of the row
-  int q = 0;                            // group-local chunk sequence number
-  for (int x = 0; conv.valid(); ++x) {
-    for (int c = 0; c < kTile / kChunkRows; ++c, ++q) {
-      const int slot = q % kRingSlots;
-      // A wait that gives up flags the CTA; the group still runs its remaining chunk
-      // sequence (without converting), so that every thread keeps meeting the group's
-      // named barriers, and every later wait returns at once.
-      bool live = c != 0 || x == 0 || wait_bar(&m->kempty[g], (x - 1) & 1, m);
-      live = live && wait_bar(&m->rawfull[g][slot], (q / kRingSlots) & 1, m);
-      if (!live) record_abort(m, p.status);
-      live = live && !aborted(m);
-      // Dequantise chunk c (rows 32c + cr) into the stage.
-      if (live) {
-      const uint8_t* rrow = ring + slot * F::CHUNK + cr * F::STRIDE;
-      const int row = c * kChunkRows + cr;
-      const uint2 codes = *reinterpret_cast<const uint2*>(rrow + F::NP * 16);
-      constexpr int PN = F::NN / 4;  // NoPE pieces per thread: 4 or 3
-      uint4 v[PN];
+  for (;;) {
+    bool progress = false;
+    if (TMA && iss.valid()) {
+      const int slot = q_issue % kRingSlots;
+      bool can = q_issue < kRingSlots || mbar_test_wait(&m->rawempty[slot], (q_issue / kRingSlots - 1) & 1);
+      can = __shfl_sync(0xffffffffu, can, 0);
+      if (can) {
+        const uint32_t base = smem_u32(ring + slot * F::SLOT);
+        const bool va = ga0 >= 0, vb = gb0 >= 0;
+        const uint32_t ba = __ballot_sync(0xffffffffu, va), bb = __ballot_sync(0xffffffffu, vb);
+        if (lane == 0) {
+          m->maskring[slot][0] = ba;
+          m->maskring[slot][1] = bb;
+          mbar_arrive_expect_tx(&m->rawfull[slot], kChunkRows * F::DATA);  // releases maskring
+        }
+        __syncwarp();
+        const int32_t ya = va ? row16(ga0) : 0, yb = vb ? row16(gb0) : 0;  // masked rows read row 0
+        int32_t y[4];
 #pragma unroll
-      for (int i = 0; i < PN; ++i) v[i] = *reinterpret_cast<const uint4*>(rrow + (cs * PN + i) * 16);
-      uint4 rp[2];
-      if (F::NR > 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) rp[i] = *reinterpret_cast<const uint4*>(rrow + (F::NN + cs * 2 + i) * 16);
+        for (int i = 0; i < 4; ++i) {
+          const int src = (4 * lane + i) & 31;
+          const int32_t a = __shfl_sync(0xffffffffu, ya, src), b = __shfl_sync(0xffffffffu, yb, src);
+          y[i] = lane < 8 ? a : b;
+        }
+        if (lane < 16)
+          tma_gather4(base + 4 * lane * F::DATA, map, F::BYTE0 / 2, y[0], y[1], y[2], y[3], &m->rawfull[slot]);
+        cp_async8(base + F::SCALES + lane * 8, scale_row(ga0));
+        cp_async8(base + F::SCALES + (lane + 32) * 8, scale_row(gb0));
+        cp_async_arrive(&m->rawfull[slot]);
+        ++q_issue;
+        iss.next(p);
+        ga0 = ga1;
+        gb0 = gb1;
+        pre.next(p);
+        ga1 = load_gidx(pre, lane);
+        gb1 = load_gidx(pre, lane + 32);
+        progress = true;
       }
-#pragma unroll
-      for (int i = 0; i < PN; ++i) {
-        const int k = cs * PN + i;
-        const int ci = F::CODE0 + (k >> 2);
-        const uint32_t code = ((ci < 4 ? codes.x : codes.y) >> (8 * (ci & 3))) & 0xFFu;
-        uint4 lo, hi;
-        dequant16_fast(v[i], code, lo, hi);
-        *reinterpret_cast<uint4*>(stage + stage_off(row, k * 16)) = lo;
-        *reinterpret_cast<uint4*>(stage + stage_off(row, k * 16 + 8)) = hi;
-      }
-      if (F::NR > 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          *reinterpret_cast<uint4*>(stage + stage_off(row, 192 + (cs * 2 + i) * 8)) = scrub_bf16x8(rp[i]);
-      }
-      if (gt == 0) m->mask[g][c] = m->maskring[g][slot];
-      }
-      named_bar_sync(bar_id, kGroupThreads);  // every thread is done with raw slot `slot`
-      if (c == 1) {
-        // The issues of this tile's chunks are all done: gbuf takes the next tile's slots.
-        m->gbuf[g][gt] = gpre;
-        skip2(pre);
-        gpre = load_gidx(pre);
-        named_bar_sync(bar_id, kGroupThreads);
-      }
-      if (iss.valid()) issue();
     }
-    fence_async_smem();
-    mbar_arrive(&m->kfull[g]);
-    skip2(conv);
+    if (qkc.valid()) {
+      bool can = false;
+      if (lane == 0) {
+        can = mbar_test_wait(&m->kfull[jq & 1], (jq >> 1) & 1) &&
+              (qkc.k == 0 ? mbar_test_wait(&m->qready, neq & 1) : mbar_test_wait(&m->sfree, (jq - 1) & 1));
+        if (can) {
+          tc_fence_after();
+          issue_qk(jq);
+        }
+      }
+      can = __shfl_sync(0xffffffffu, can, 0);
+      if (can) {
+        const bool item_end = qkc.k + 1 == qkc.n;
+        ++jq;
+        qkc.next(p);
+        neq += item_end ? 1 : 0;
+        progress = true;
+      }
+    }
+    if (pvc.valid() && jp < jq) {
+      bool can = false;
+      if (lane == 0) {
+        can = mbar_test_wait(&m->pfull, jp & 1);
+        if (can) {
+          tc_fence_after();
+          issue_pv(jp, pvc.k == 0);
+          if (pvc.k + 1 == pvc.n) umma_commit(&m->odone);
+        }
+      }
+      can = __shfl_sync(0xffffffffu, can, 0);
+      if (can) {
+        ++jp;
+        pvc.next(p);
+        progress = true;
+      }
+    }
+    if (!(TMA && iss.valid()) && !qkc.valid() && !pvc.valid()) break;
+    if (progress) {
+      idle_since = 0;
+    } else {
+      if (aborted(m)) break;
+      const uint64_t now = globaltimer_ns();
+      if (idle_since == 0) {
+        idle_since = now;
+      } else if (now - idle_since > kWaitLimitNs) {
+        if (lane == 0) record_abort(m, p.status);
+        break;
+      }
+      // Nothing ready: sleep on the P buffer of the oldest pending PV (the event the
+      // critical path waits for), or briefly when no PV is pending.
+      if (pvc.valid() && jp < jq)
+        (void)mbar_try_wait_hint(&m->pfull, jp & 1, 1000);
+      else
+        __nanosleep(64);
+    }
+  }
+  if (lane == 0) {
+    umma_commit(&m->drain);  // every issued UMMA lands before TMEM is freed
+    mbar_wait_bounded(&m->drain, 0, kWaitLimitNs);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after the CTA is gone
+  __syncwarp();
+}
+
+// The converter warps (9-15, ct = 0..223) of the TMA mode: each raw chunk the control
+// warp put in flight is dequantised into the stage of its tile.
+
+template <int HALF>
+__device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int items, int ct) {
+  using F = RawFmt<HALF>;
+  uint8_t* ring = smem + kOffRing;
+  ChunkCursor conv;
+  conv.init(p, cid, p.G, items);
+  for (int q = 0; conv.valid(); ++q) {
+    const int slot = q % kRingSlots;
+    const int c = conv.c;
+    const int j = q >> 1;   // tile sequence number
+    const int s = j & 1;    // its stage
+    uint8_t* stage = smem + s * kStageBytes;
+    // A wait that gives up flags the CTA; the converters still run their remaining chunk
+    // sequence without converting, and every later wait returns at once.
+    bool live = c != 0 || j < 2 || wait_bar(&m->kempty[s], ((j >> 1) - 1) & 1, m);
+    live = live && wait_bar(&m->rawfull[slot], (q / kRingSlots) & 1, m);
+    if (!live) record_abort(m, p.status);
+    live = live && !aborted(m);
+    if (live) {
+      const uint8_t* raw = ring + slot * F::SLOT;
+      const uint32_t mk0 = m->maskring[slot][0], mk1 = m->maskring[slot][1];
+      auto valid_row = [&](int r) { return (((r < 32 ? mk0 : mk1) >> (r & 31)) & 1u) != 0u; };
+      // NoPE: 64 rows x NN pieces; consecutive threads take consecutive pieces of a row.
+      // The pieces are loaded first, then converted on the fast path unless a piece of
+      // the warp needs the exact one.
+      constexpr int NI = (kChunkRows * F::NN + kConverters - 1) / kConverters;
+      uint4 v[NI];
+      uint32_t code[NI];
+      bool clean = true;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int pc = ct + kConverters * i;
+        const int r = pc / F::NN, k = pc - r * F::NN;
+        v[i] = make_uint4(0, 0, 0, 0);
+        code[i] = 0;
+        if (pc < kChunkRows * F::NN) {
+          v[i] = *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16);
+          code[i] = raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)];
+          clean = clean && code[i] <= 134u && fp8x16_no_nan(v[i]);
+        }
+      }
+      const bool fast = __all_sync(0xffffffffu, clean);
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int pc = ct + kConverters * i;
+        const int r = pc / F::NN, k = pc - r * F::NN;
+        if (pc < kChunkRows * F::NN) {
+          if (fast)
+            convert_nope<true>(stage, c * kChunkRows + r, k, v[i], code[i], valid_row(r));
+          else
+            convert_nope<false>(stage, c * kChunkRows + r, k, v[i], code[i], valid_row(r));
+        }
+      }
+      if constexpr (F::NR > 0) {
+#pragma unroll
+        for (int i = 0; i < (kChunkRows * F::NR + kConverters - 1) / kConverters; ++i) {
+          const int pc = ct + kConverters * i;
+          if (pc < kChunkRows * F::NR) {
+            const int r = pc / F::NR, k = pc - r * F::NR;
+            uint4 v = *reinterpret_cast<const uint4*>(raw + r * F::DATA + (F::NN + k) * 16);
+            if (!valid_row(r)) v = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(stage + stage_off(c * kChunkRows + r, 192 + k * 8)) = scrub_bf16x8(v);
+          }
+        }
+      }
+      if (ct == 0) {
+        m->mask[s][2 * c] = mk0;
+        m->mask[s][2 * c + 1] = mk1;
+      }
+    }
+    mbar_arrive(&m->rawempty[slot]);
+    if (c == 1) {
+      fence_async_smem();
+      mbar_arrive(&m->kfull[s]);
+    }
+    conv.next(p);
+  }
+}
+
+// Fallback producer for caches whose rows are only 8-byte aligned (pages of an odd slot
+// count) or too large for 32-bit TMA row coordinates: every thread loads its pieces
+// straight from global memory (no ring), one 64-row chunk at a time.
+template <int HALF>
+__device__ __forceinline__ void produce_direct(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int items,
+                                               int ct) {
+  using F = RawFmt<HALF>;
+  const CacheView cv = make_cache_view(p.cache, p.P);
+  const int64_t n_slots = p.num_pages * p.P;
+  ChunkCursor conv;
+  conv.init(p, cid, p.G, items);
+  for (int q = 0; conv.valid(); ++q) {
+    const int c = conv.c;
+    const int j = q >> 1;
+    const int s = j & 1;
+    uint8_t* stage = smem + s * kStageBytes;
+    bool live = c != 0 || j < 2 || wait_bar(&m->kempty[s], ((j >> 1) - 1) & 1, m);
+    if (!live) record_abort(m, p.status);
+    live = live && !aborted(m);
+    auto slot_of = [&](int r) -> int32_t {
+      if (r >= conv.rows()) return -1;
+      const int32_t v = ldg_nc_s32(p.gidx + conv.row0() + r);
+      return ((int64_t)v >= n_slots) ? -1 : v;
+    };
+    if (live) {
+      for (int pc = ct; pc < kChunkRows * F::NP; pc += kConverters) {
+        const int r = pc / F::NP, k = pc - r * F::NP;
+        const int32_t g = slot_of(r);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        uint32_t code = 0;
+        if (g >= 0) {
+          const uint8_t* d = row_data(cv, g) + F::BYTE0 + k * 16;
+          const uint2 a = ldg_nc_v2(d), b = ldg_nc_v2(d + 8);
+          v = make_uint4(a.x, a.y, b.x, b.y);
+          if (k < F::NN) code = ldg_nc_u8(row_scales(cv, g) + F::CODE0 + (k >> 2));
+        }
+        if (k < F::NN)
+          convert_nope<false>(stage, c * kChunkRows + r, k, v, code, g >= 0);
+        else
+          *reinterpret_cast<uint4*>(stage + stage_off(c * kChunkRows + r, 192 + (k - F::NN) * 8)) = scrub_bf16x8(v);
+      }
+      if (ct < 64) {  // valid-row masks of the chunk's two 32-row quarters
+        const uint32_t bits = __ballot_sync(0xffffffffu, slot_of(ct) >= 0);
+        if ((ct & 31) == 0) m->mask[s][2 * c + (ct >> 5)] = bits;
+      }
+    }
+    if (c == 1) {
+      fence_async_smem();
+      mbar_arrive(&m->kfull[s]);
+    }
+    conv.next(p);
+  }
 }
 
 }  // namespace
 
-template <bool ALIGN16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pair_kernel(AttnParams p) {
+// Kernel parameters: the call's parameters and, for the TMA producer, the cache's two
+// gather tensor maps (one per latent half).
+struct KernelParams {
+  AttnParams p;
+  CUtensorMap map[2];  // the type carries the 128-byte alignment of a tensor map
+};
+
+template <bool TMA>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_pair_kernel(const __grid_constant__ KernelParams kp) {
+  const AttnParams& p = kp.p;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   uint8_t* sP = smem + kOffP;
@@ -424,9 +648,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&m->kfull[s], kGroupThreads);
+      mbar_init(&m->kfull[s], kConverters);
       mbar_init(&m->kempty[s], 1);
-      for (int r = 0; r < kRingSlots; ++r) mbar_init(&m->rawfull[s][r], kGroupThreads);
+    }
+    for (int r = 0; r < kRingSlots; ++r) {
+      mbar_init(&m->rawfull[r], 1 + 32);  // the loader's expect-tx + its 32 lanes' scale copies
+      mbar_init(&m->rawempty[r], kConverters);
     }
     mbar_init(&m->sfull, 1);
     mbar_init(&m->sfree, kSoftmaxThreads);
@@ -437,6 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
     mbar_init(&m->odone, 1);
     mbar_init(&m->drain, 1);
     mbar_init(&m->sgrp, kSoftmaxThreads);
+    mbar_init(&m->qready, kSoftmaxThreads);
     for (int i = 0; i < 4; ++i) mbar_init(&m->hpair[i], 64);
     m->abort = 0;
     fence_mbar_init();
@@ -461,48 +689,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
     const int h = tid & 127;
     const int hc = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const bool issuer = tid == 0;
-    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTile, false, false);
-    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDHalf, false, true);
-    const uint32_t a_stage = smem_u32(smem);
-    const uint32_t a_p = smem_u32(sP);
-    // Exchange regions and the peer's barriers are recomputed at each use (kernel
-    // parameters live in the constant bank), which keeps them out of the register budget.
-    auto xregion = [&](uint32_t rank) { return p.xchg + ((size_t)cid * 2 + rank) * kXchgRegion; };
     const float sl2 = p.scale * kLog2e;
+    // Exchange regions are recomputed at each use (kernel parameters live in the constant
+    // bank), which keeps them out of the register budget.
+    auto xregion = [&](uint32_t rank) { return p.xchg + ((size_t)cid * 2 + rank) * kXchgRegion; };
     bool ok = true;
     uint32_t sgrp_phase = 0;
     int j = 0;       // tile sequence number (runs on across items)
-    int it_no = 0;   // items taken by this pair so far
+    int ne_no = 0;   // items with tiles taken by this pair so far
 
-    auto issue_qk = [&](int jj) {  // S = Q K^T for tile jj
-      const uint32_t base = a_stage + (jj & 1) * kStageBytes;
-#pragma unroll
-      for (int kk = 0; kk < kDHalf / 16; ++kk)
-        umma_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_sw128(base + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
-                kIdescQK, kk > 0 ? 1u : 0u);
-      umma_commit(&m->sfull);
-    };
-    auto issue_pv = [&](int jj, bool first) {  // O += P V for tile jj, then free its stage and P
-      const uint32_t base = a_stage + (jj & 1) * kStageBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        umma_ss(tmem + kColO, desc_sw128(a_p + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
-                desc_sw128(base + kk * 2048, kSlab, 1024), kIdescPV, (!first || kk > 0) ? 1u : 0u);
-      umma_commit(&m->kempty[jj & 1]);
-      umma_commit(&m->pvdone);
-    };
-
-    for (int w = cid; w < items && ok; w += p.G, ++it_no) {
+    for (int w = cid; w < items && ok; w += p.G) {
       const Item item = item_of(p, w);
       const int n = item.n;
       {  // this thread's half of head h's Q half -> TMEM columns [64 hc, 64 hc + 64) of lane h
         const uint8_t* qrow = static_cast<const uint8_t*>(p.q) + ((int64_t)item.t * p.H + h) * (kLatent * 2) +
                               half * (kDHalf * 2) + hc * 256;
         uint32_t r[2][32];
+        // local dims [64 hc, 64 hc + 64)... of this CTA's 256: NoPE below local dim 448 - 256 half
+        const int nope_chunks = half == 0 ? 16 : (hc == 0 ? 16 : 8);  // 16-byte chunks of NoPE dims
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint4 v = h < p.H ? ldg_nc_v4(qrow + i * 16) : make_uint4(0, 0, 0, 0);
+          uint4 v = h < p.H ? ldg_nc_v4(qrow + i * 16) : make_uint4(0, 0, 0, 0);
+          if (i < nope_chunks) {  // the stage's (d0, d2, d1, d3) order of NoPE dims
+            v = make_uint4(__byte_perm(v.x, v.y, 0x5410u), __byte_perm(v.x, v.y, 0x7632u),
+                           __byte_perm(v.z, v.w, 0x5410u), __byte_perm(v.z, v.w, 0x7632u));
+          }
           r[i >> 3][(i & 7) * 4 + 0] = v.x;
           r[i >> 3][(i & 7) * 4 + 1] = v.y;
           r[i >> 3][(i & 7) * 4 + 2] = v.z;
@@ -512,20 +723,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
         tmem_st32(tmem + lane_base + kColQ + hc * 64 + 32, r[1]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&m->sgrp);
-        ok = wait_bar_warp(&m->sgrp, sgrp_phase, m);
-        sgrp_phase ^= 1u;
-        tc_fence_after();
+        if (n > 0) mbar_arrive(&m->qready);  // the issuer may start QK of the item's first tile
       }
-      if (ok && issuer && n > 0) {
-        if ((ok = wait_bar(&m->kfull[j & 1], (j >> 1) & 1, m))) {
-          tc_fence_after();
-          issue_qk(j);
-        } else {
-          record_abort(m, p.status);
-        }
-      }
-      ok = __all_sync(0xffffffffu, ok);
 
       float m_ref = -INFINITY;  // reference max (log2 domain) the weights are taken against
       float l_run = 0.f;        // this thread's share of the denominator relative to m_ref
@@ -543,65 +742,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
           for (int i = 0; i < 32; ++i) x[c2 * 32 + i] = __uint_as_float(r[i]) * sl2;
         }
         // S is in registers: QK of the next tile may go as soon as every thread has
-        // loaded S and the next stage is filled.  The issuer only probes here and at
-        // the later checkpoints, so its own exchange traffic never waits on producers.
+        // loaded S and the next stage is filled.
         tc_fence_before();
         mbar_arrive(&m->sfree);
-        bool qk_pending = issuer && k + 1 < n;
-        auto try_qk_next = [&]() {
-          if (qk_pending && mbar_test_wait(&m->sfree, j & 1) &&
-              mbar_test_wait(&m->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
-            tc_fence_after();
-            issue_qk(j + 1);
-            qk_pending = false;
-          }
-        };
-        try_qk_next();
-        __syncwarp();
 
-        // Send this thread's 64 partials (log2 units) to the peer.
+        // Exchange.  The peer's partials land in this thread's 128-byte slice of the P
+        // buffer, which is free from the end of PV of the previous tile until this tile's
+        // P is written: say so to the peer, then send this thread's partials (log2 units,
+        // int16 fixed point) into the peer's slice of the same thread over DSMEM.  A block
+        // beyond the fixed-point range goes through the L2 exchange buffer as fp32.
+        if (j > 0 && !(ok = wait_bar_warp(&m->pvdone, (j - 1) & 1, m))) break;
+        tc_fence_after();
+        mbar_arrive_cluster(mapa(smem_u32(&m->xempty), peer));
+        uint8_t* slice = sP + hc * kSlab;
         float amax = 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) amax = fmaxf(amax, fabsf(x[c]));
         const bool fixed = amax <= kFixedMax;  // false for NaN too: those go as fp32
-        if (j > 0 && !(ok = wait_bar_warp(&m->xempty, (j - 1) & 1, m, true))) break;
-        uint8_t* xpeer = xregion(peer);
-        uint8_t* dst = xpeer + tid * 16;
+        if (!(ok = wait_bar_warp(&m->xempty, j & 1, m, true))) break;
+        const uint32_t peer_slice = mapa(smem_u32(slice), peer);
         if (fixed) {
           const float enc = amax > 0.f ? kQMax / amax : 0.f;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            st_global_v4(dst + i * (kSoftmaxThreads * 16), pack_q16(x[8 * i], x[8 * i + 1], enc),
-                         pack_q16(x[8 * i + 2], x[8 * i + 3], enc), pack_q16(x[8 * i + 4], x[8 * i + 5], enc),
-                         pack_q16(x[8 * i + 6], x[8 * i + 7], enc));
+            st_cluster_v4(peer_slice + sw128_off(h, i), pack_q16(x[8 * i], x[8 * i + 1], enc),
+                          pack_q16(x[8 * i + 2], x[8 * i + 3], enc), pack_q16(x[8 * i + 4], x[8 * i + 5], enc),
+                          pack_q16(x[8 * i + 6], x[8 * i + 7], enc));
         } else {
+          uint8_t* dst = xregion(peer) + tid * 16;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             st_global_v4(dst + i * (kSoftmaxThreads * 16), __float_as_uint(x[4 * i]), __float_as_uint(x[4 * i + 1]),
                          __float_as_uint(x[4 * i + 2]), __float_as_uint(x[4 * i + 3]));
         }
-        reinterpret_cast<float*>(xpeer + kXchgData)[tid] = fixed ? amax / kQMax : -1.f;
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mapa(smem_u32(&m->xscale[tid]), peer)),
+                     "f"(fixed ? amax / kQMax : -1.f)
+                     : "memory");
         mbar_arrive_cluster(mapa(smem_u32(&m->xfull), peer));
-        try_qk_next();
-        __syncwarp();
 
-        // Receive the peer's partials.  This thread's 128-byte slice of the P buffer is
-        // free once PV of the previous tile is done, until it takes this tile's P: the
-        // slice stages the peer's int16 partials (cp.async from L2), so the exchange buffer
-        // is released at once and the decode holds one piece in registers at a time.
-        if (j > 0 && !(ok = wait_bar_warp(&m->pvdone, (j - 1) & 1, m))) break;
-        tc_fence_after();
+        // Receive the peer's partials and add them.
         if (!(ok = wait_bar_warp(&m->xfull, j & 1, m, true))) break;
         {
-          const uint8_t* xown = xregion(half);
-          const uint8_t* src = xown + tid * 16;
-          uint8_t* slice = sP + hc * kSlab;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cp_async16(smem_u32(slice + sw128_off(h, i)), src + i * (kSoftmaxThreads * 16));
-          const float dec = ld_global_cg_f32(xown + kXchgData + tid * 4);
-          asm volatile("cp.async.wait_all;" ::: "memory");
+          const float dec = m->xscale[tid];
           if (dec >= 0.f) {
-            mbar_arrive_cluster(mapa(smem_u32(&m->xempty), peer));
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const uint4 v = *reinterpret_cast<const uint4*>(slice + sw128_off(h, i));
@@ -613,33 +796,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
               }
             }
           } else {
-            // fp32 partials (a block beyond the fixed-point range): the staged first half
-            // holds columns 0..31; the slice then stages columns 32..63.
+            // fp32 partials from the L2 buffer, staged through the slice 8 pieces at a time
+            const uint8_t* src = xregion(half) + tid * 16;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint4 v = *reinterpret_cast<const uint4*>(slice + sw128_off(h, i));
-              x[4 * i] += __uint_as_float(v.x);
-              x[4 * i + 1] += __uint_as_float(v.y);
-              x[4 * i + 2] += __uint_as_float(v.z);
-              x[4 * i + 3] += __uint_as_float(v.w);
-            }
+            for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              cp_async16(smem_u32(slice + sw128_off(h, i)), src + (8 + i) * (kSoftmaxThreads * 16));
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            mbar_arrive_cluster(mapa(smem_u32(&m->xempty), peer));
+              for (int i = 0; i < 8; ++i)
+                cp_async16(smem_u32(slice + sw128_off(h, i)), src + (8 * hb + i) * (kSoftmaxThreads * 16));
+              asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint4 v = *reinterpret_cast<const uint4*>(slice + sw128_off(h, i));
-              x[32 + 4 * i] += __uint_as_float(v.x);
-              x[32 + 4 * i + 1] += __uint_as_float(v.y);
-              x[32 + 4 * i + 2] += __uint_as_float(v.z);
-              x[32 + 4 * i + 3] += __uint_as_float(v.w);
+              for (int i = 0; i < 8; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(slice + sw128_off(h, i));
+                x[32 * hb + 4 * i] += __uint_as_float(v.x);
+                x[32 * hb + 4 * i + 1] += __uint_as_float(v.y);
+                x[32 * hb + 4 * i + 2] += __uint_as_float(v.z);
+                x[32 * hb + 4 * i + 3] += __uint_as_float(v.w);
+              }
             }
           }
         }
-        try_qk_next();
-        __syncwarp();
 
         // The stage's valid-row masks (published by the producers before kfull).
         if (!(ok = wait_bar_warp(&m->kfull[s], (j >> 1) & 1, m))) break;
@@ -698,30 +873,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(&m->pfull);
-        if (issuer) {
-          try_qk_next();
-          if ((ok = wait_bar(&m->pfull, j & 1, m))) {
-            tc_fence_after();
-            issue_pv(j, k == 0);
-            if (k + 1 == n) umma_commit(&m->odone);
-          }
-          // PV of this tile frees its stage for the producers first; then QK of the next
-          // tile, if it is still pending, waits for its stage here.
-          if (ok && qk_pending) {
-            if ((ok = wait_bar(&m->sfree, j & 1, m)) &&
-                (ok = wait_bar(&m->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1, m))) {
-              tc_fence_after();
-              issue_qk(j + 1);
-              qk_pending = false;
-            }
-          }
-          if (!ok) record_abort(m, p.status);
-        }
-        ok = __all_sync(0xffffffffu, ok && !aborted(m));
+        ok = !aborted(m);
       }
       if (!ok) break;
-      if (issuer && n == 0) mbar_arrive(&m->odone);
-      if (!(ok = wait_bar_warp(&m->odone, it_no & 1, m))) break;
+      if (n > 0) {
+        if (!(ok = wait_bar_warp(&m->odone, ne_no & 1, m))) break;
+        ++ne_no;
+      }
       // Epilogue: head h, local dims [128 hc, 128 hc + 128) of this CTA's 256.
       tc_fence_after();
       m->red[0][hc][h] = l_run;  // every use of red[][] by the tile loop is over (odone)
@@ -757,6 +915,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
         if (o_live) {
           tmem_ld32(tmem + lane_base + kColO + hc * 128 + cc * 32, o);
           tmem_wait_ld();
+          // NoPE columns hold dims in the (d0, d2, d1, d3) order of the stage
+          if (d0 + cc * 32 < kNope) {
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+              const uint32_t t1 = o[4 * g4 + 1];
+              o[4 * g4 + 1] = o[4 * g4 + 2];
+              o[4 * g4 + 2] = t1;
+            }
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
@@ -792,22 +959,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_pa
       sgrp_phase ^= 1u;
       tc_fence_after();
     }
-    if (!ok) {
-      record_abort(m, p.status);
-      if (issuer) {
-        umma_commit(&m->drain);  // let issued UMMAs land before TMEM is freed
-        mbar_wait_bounded(&m->drain, 0, kWaitLimitNs);
-      }
-    }
+    if (!ok) record_abort(m, p.status);
   } else {
     regs_dec<kProducerRegs>();
     // ------------------------------------------------------------ gather + dequant
     const int pt = tid - kSoftmaxThreads;
-    const int g = pt >> 7;
-    if (half == 0)
-      produce<0, ALIGN16>(smem, m, p, cid, items, g, pt & 127);
-    else
-      produce<1, ALIGN16>(smem, m, p, cid, items, g, pt & 127);
+    if (pt < 32) {
+      if (half == 0)
+        control_warp<0, TMA>(smem, m, p, &kp.map[0], cid, items, tmem, pt);
+      else
+        control_warp<1, TMA>(smem, m, p, &kp.map[1], cid, items, tmem, pt);
+    } else if constexpr (TMA) {
+      if (half == 0)
+        produce_tma<0>(smem, m, p, cid, items, pt - 32);
+      else
+        produce_tma<1>(smem, m, p, cid, items, pt - 32);
+    } else {
+      if (half == 0)
+        produce_direct<0>(smem, m, p, cid, items, pt - 32);
+      else
+        produce_direct<1>(smem, m, p, cid, items, pt - 32);
+    }
   }
 
   // Wind down: nobody may leave while the peer can still arrive on this CTA's barriers,
@@ -830,26 +1002,70 @@ int attn_pairs(int64_t items, int sms) {
 
 size_t attn_xchg_bytes(int pairs) { return (size_t)pairs * 2 * kXchgRegion; }
 
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The cache as a 2-D tensor of u16 whose row y covers bytes [16y, 16y + 576) (every data
+// row of the cache starts at a multiple of 16 bytes when P * 584 is one); a gather box
+// of one row covers the half's bytes.  False when the view does not apply.
+bool make_gather_maps(const AttnParams& p, CUtensorMap* maps) {
+  if (((int64_t)p.P * kRowBytes) % 16 != 0 || (reinterpret_cast<uintptr_t>(p.cache) & 15u) != 0) return false;
+  const int64_t bytes = p.num_pages * p.P * kRowBytes;
+  const int64_t rows = (bytes - kDataBytes) / 16 + 1;
+  if (rows < 1 || rows >= ((int64_t)1 << 31)) return false;
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t gdim[2] = {(cuuint64_t)(kDataBytes / 2), (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {16};
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint32_t box0[2] = {(cuuint32_t)(RawFmt<0>::DATA / 2), 1};
+  const cuuint32_t box1[2] = {(cuuint32_t)(RawFmt<1>::DATA / 2), 1};
+  void* base = const_cast<uint8_t*>(p.cache);
+  return enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box0, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+         enc(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box1, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
-  const bool align16 = ((int64_t)p.P * kRowBytes) % 16 == 0;
+  KernelParams kp;
+  kp.p = p;
+  const bool tma = make_gather_maps(p, kp.map);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static bool attr_done[2][64] = {};
-  if (dev < 64 && !attr_done[align16][dev]) {
-    e = align16 ? cudaFuncSetAttribute(attn_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes)
-                : cudaFuncSetAttribute(attn_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  if (dev < 64 && !attr_done[tma][dev]) {
+    e = tma ? cudaFuncSetAttribute(attn_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBytes)
+            : cudaFuncSetAttribute(attn_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[align16][dev] = true;
+    attr_done[tma][dev] = true;
   }
   const dim3 grid(2 * p.G, 1);
-  if (align16)
-    attn_pair_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+  if (tma)
+    attn_pair_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(kp);
   else
-    attn_pair_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
+    attn_pair_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(kp);
   return cudaGetLastError();
 }
 

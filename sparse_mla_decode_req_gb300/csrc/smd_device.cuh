@@ -157,6 +157,50 @@ __device__ __forceinline__ void dequant16_fast(uint4 in, uint32_t code, uint4& l
   hi = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
+// Attention-stage dequantisation: the same values as dequant16_fast, with the elements of
+// every group of four dims stored in the order (d0, d2, d1, d3) -- the order in which
+// they fall out of placing the four bytes of a 32-bit word in two bf16x2 words.  The
+// attention kernel stores Q in the same order, so Q.K is unchanged, and it restores the
+// order of O.  Fast path (warp-uniform): no NaN byte and code <= 134, so that one exact
+// multiply by 2^(code - 7) carries both the 2^120 of the placement and the scale.
+__device__ __forceinline__ void place4(uint32_t w, uint32_t& d02, uint32_t& d13) {
+  d02 = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
+  d13 = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
+}
+// True when the 16 bytes hold no NaN encoding (low 7 bits all ones).
+__device__ __forceinline__ bool fp8x16_no_nan(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t hit = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hit |= (w[i] & 0x7F7F7F7Fu) + 0x01010101u;
+  return (hit & 0x80808080u) == 0u;
+}
+__device__ __forceinline__ void dequant16_perm_fast(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
+  const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
+  const uint32_t sc = sb | (sb << 16);
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a, b;
+    place4(w[i], a, b);
+    r[2 * i] = mul_bf16x2(a, sc);
+    r[2 * i + 1] = mul_bf16x2(b, sc);
+  }
+  lo = make_uint4(r[0], r[1], r[2], r[3]);
+  hi = make_uint4(r[4], r[5], r[6], r[7]);
+}
+// Any input (NaN bytes, large or NaN codes): the exact path, then the same reordering.
+__device__ __forceinline__ void dequant16_perm_exact(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
+  dequant16_fast(in, code, lo, hi);
+  const uint32_t a0 = __byte_perm(lo.x, lo.y, 0x5410u), a1 = __byte_perm(lo.x, lo.y, 0x7632u);
+  const uint32_t a2 = __byte_perm(lo.z, lo.w, 0x5410u), a3 = __byte_perm(lo.z, lo.w, 0x7632u);
+  const uint32_t b0 = __byte_perm(hi.x, hi.y, 0x5410u), b1 = __byte_perm(hi.x, hi.y, 0x7632u);
+  const uint32_t b2 = __byte_perm(hi.z, hi.w, 0x5410u), b3 = __byte_perm(hi.z, hi.w, 0x7632u);
+  lo = make_uint4(a0, a1, a2, a3);
+  hi = make_uint4(b0, b1, b2, b3);
+}
+
 __device__ __forceinline__ uint4 scrub_bf16x8(uint4 v) {
   v.x = scrub_bf16x2(v.x);
   v.y = scrub_bf16x2(v.y);
@@ -248,6 +292,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+// try_wait with a caller-chosen suspend-time hint (ns).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
