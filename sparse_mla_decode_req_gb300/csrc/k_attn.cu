@@ -1036,10 +1036,10 @@ bool make_gather_maps(const AttnParams& p, CUtensorMap* maps) {
   const cuuint32_t box1[2] = {(cuuint32_t)(RawFmt<1>::DATA / 2), 1};
   void* base = const_cast<uint8_t*>(p.cache);
   return enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box0, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
          enc(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box1, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace
