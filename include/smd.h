@@ -116,9 +116,9 @@ SMD_API size_t smd_workspace_size(const smd_dims *dims, int num_splits, int num_
 /*
  * Device bytes of the exchange buffers smd_sparse_mla_attention needs: the two CTAs that
  * share a (token, split) work item each hold half of the 512 latent dims, and swap their
- * partial QK scores of every 128-entry tile through these buffers (about 65 KB per CTA,
- * one CTA pair per two SMs, at most min(T * S, num_sms / 2) pairs).  The content is
- * scratch: nothing is read before the same call writes it.  Returns 0 on bad dims.
+ * fp32 partial QK scores of every 64-entry tile through these buffers (two 32 KB buffers
+ * per CTA, one CTA pair per two SMs, at most min(T * S, num_sms / 2) pairs).  The content
+ * is scratch: nothing is read before the same call writes it.  Returns 0 on bad dims.
  */
 SMD_API size_t smd_attention_xchg_size(const smd_dims *dims, int num_splits, int num_sms);
 

@@ -70,7 +70,7 @@ def test_split_selector_rules(lib):
     assert api.select_num_splits(_dims(), 0, 152) == api.select_num_splits(_dims(), 0, 152)
 
 
-XCHG_PER_CTA = 16 * 256 * 16 + 256 * 4   # 16 pieces x 256 softmax threads x 16 B, then one scale each
+XCHG_PER_CTA = 2 * 256 * 32 * 4   # two buffers x 256 softmax threads x 32 fp32 partial scores
 
 
 def _xchg(items, sms):
