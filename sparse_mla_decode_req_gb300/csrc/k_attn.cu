@@ -26,13 +26,14 @@
 // producers prefetch the next item's rows while the current one finishes.
 //
 // Roles (512 threads):
-//   warp 8, the MMA warp: issues every UMMA from one lane, in order, each after a
-//     blocking wait for its inputs: S_c(j) = Q_c K_c(j)^T (M128 N64 K256, A from TMEM)
-//     into S buffer j&1, and O_c += P(j) V_c(j) (M128 N256 K64, the stage read MN-major).
-//   warp 9, the loader: puts each tile's raw rows in flight with TMA row gathers (four
+//   warps 8 and 9, the MMA warps: issue every UMMA from one lane each, after blocking
+//     waits for their inputs: S_c(j) = Q_c K_c(j)^T (M128 N64 K256, A from TMEM) into S
+//     buffer j&1 (warp 8), and O_c += P(j) V_c(j) (M128 N256 K64, the stage read
+//     MN-major; warp 9, which also forwards the exchange events to the peer CTA).
+//   warp 10, the loader: puts each tile's raw rows in flight with TMA row gathers (four
 //     rows per gather, the CTA's half of every 576-byte data row) and 8-byte scale-row
 //     copies into the raw ring.
-//   warps 10-15, the converters: dequantise each raw tile into its stage.
+//   warps 11-15, the converters: dequantise each raw tile into its stage.
 //   warps 0-7, softmax + epilogue: thread (h, hc) owns head h (TMEM lane h) and score
 //     columns [32 hc, 32 hc + 32) of every tile.
 //
@@ -101,21 +102,23 @@ constexpr uint32_t kXchgBuf = kCols * 4u * kSoftmaxThreads;  // 32 KB
 constexpr uint32_t kXchgRegion = 2u * kXchgBuf;
 
 struct Misc {
-  uint64_t kfull[kStages];   // converters -> issuer, softmax: stage filled (one arrival per converter)
+  uint64_t kfull[kStages];   // converters -> issuer, softmax: stage filled (one arrival per warp)
   uint64_t kempty[kStages];  // PV commit -> converters: stage consumed
   uint64_t sfull[2];         // QK commit -> softmax: S buffer filled
-  uint64_t sfree[2];         // softmax -> issuer: S buffer loaded into registers (256)
-  uint64_t pfull[2];         // softmax -> issuer: P buffer written, O rescaled (256)
+  uint64_t sfree[2];         // softmax -> issuer: S buffer loaded into registers (8 warps)
+  uint64_t pfull[2];         // softmax -> issuer: P buffer written, O rescaled (8 warps)
   uint64_t pvdone[2];        // PV commit -> softmax: P buffer read, O updated
-  uint64_t xfull[2];         // peer softmax -> softmax: peer partials in my exchange buffer (256 remote)
-  uint64_t xempty[2];        // peer softmax -> softmax: peer has read my partials (256 remote)
+  uint64_t xsent[2];         // softmax -> PV warp: partials of a tile stored to L2 (8 warps)
+  uint64_t xread[2];         // softmax -> PV warp: the peer's partials of a tile consumed (8 warps)
+  uint64_t xfull[2];         // peer PV warp -> softmax: peer partials in my exchange buffer (1 remote)
+  uint64_t xempty[2];        // peer PV warp -> softmax: peer has read my partials (1 remote)
   uint64_t odone;            // last PV commit of an item -> softmax: O final
-  uint64_t drain;            // issuer self-drain before TMEM is freed after a failed wait
-  uint64_t sgrp;             // softmax-group rendezvous (256 arrivals per use)
-  uint64_t qready;           // softmax -> issuer: an item's Q is in TMEM (256 arrivals)
+  uint64_t drain[2];         // the MMA warps' self-drain before TMEM is freed
+  uint64_t sgrp;             // softmax-group rendezvous (8 warps per use)
+  uint64_t qready;           // softmax -> issuer: an item's Q is in TMEM (8 warps)
   uint64_t rawfull[kRingSlots];   // raw tile landed (loader expect-tx + 32 scale-copy arrivals)
-  uint64_t rawempty[kRingSlots];  // raw tile converted (one arrival per converter)
-  uint64_t hpair[4];         // warps w and w+4 (the two threads of heads 32w..32w+31): 64
+  uint64_t rawempty[kRingSlots];  // raw tile converted (one arrival per converter warp)
+  uint64_t hpair[4];         // warps w and w+4 (the two threads of heads 32w..32w+31): 2
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t mask[kStages][2];        // valid-row bit masks of each stage's 32-row halves
@@ -136,24 +139,46 @@ __device__ __forceinline__ bool aborted(const Misc* m) {
 }
 
 // Bounded wait that also gives up early once another role of this CTA has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Misc* m,
-                                         bool cluster_acquire = false) {
+__device__ __forceinline__ bool wait_bar_loop(uint64_t* bar, uint32_t parity, const Misc* m, bool cluster_acquire) {
   auto poll = [&]() { return cluster_acquire ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!poll()) {
     if (aborted(m) || globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
   return true;
 }
+// The producer warps' waits: first poll inline, the rest in one out-of-line copy, which
+// keeps their many wait sites from filling the instruction cache.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, const Misc* m, bool cluster_acquire) {
+  return wait_bar_loop(bar, parity, m, cluster_acquire);
+}
+template <bool OUTLINE = false>
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Misc* m,
+                                         bool cluster_acquire = false) {
+  if (cluster_acquire ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  if constexpr (OUTLINE)
+    return wait_bar_slow(bar, parity, m, cluster_acquire);
+  else
+    return wait_bar_loop(bar, parity, m, cluster_acquire);
+}
 
 // The same wait done by a whole warp, with a warp-uniform result, so that a warp never
 // splits into lanes that go on and lanes that leave (which would strand the first at the
 // next warp-collective instruction).
+template <bool OUTLINE = false>
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, const Misc* m,
                                               bool cluster_acquire = false) {
-  const bool r = wait_bar(bar, parity, m, cluster_acquire);
+  const bool r = wait_bar<OUTLINE>(bar, parity, m, cluster_acquire);
   return __all_sync(0xffffffffu, r);
+}
+
+// One arrival per warp: the warp's lanes converge (which orders their earlier memory
+// accesses before lane 0's release), then lane 0 arrives.  Barriers that whole warps
+// arrive on count warps, which keeps the per-tile shared-memory atomics (each arrival is
+// one) from congesting the shared-memory pipe the converters and the softmax use.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ void record_abort(Misc* m, uint32_t* status) {
@@ -267,84 +292,104 @@ __device__ __forceinline__ void convert_nope(uint8_t* stage, int srow, int k, ui
   *reinterpret_cast<uint4*>(stage + stage_off(srow, k * 16 + 8)) = hi;
 }
 
-constexpr int kConverters = kProducerThreads - 64;  // warps 10-15
+constexpr int kConverters = kProducerThreads - 96;  // warps 11-15
 
-// The MMA warp (warp 8): issues every UMMA of the CTA from lane 0, in the order the
-// skewed softmax consumes them (QK of tile j + 1 before PV of tile j, whose P is written
-// after S(j + 1) is loaded), each after a blocking wait for its inputs: QK once the stage
-// is filled and its S buffer free (an item's first QK once the item's Q is in TMEM), PV
-// once P is written; the last PV of an item also signals O final.
+
+// The MMA warps issue every UMMA of the CTA from one lane, each after a blocking wait for
+// its inputs, in the order in which the skewed softmax frees them.
+//   warp 8 (QK): QK of a tile once its stage is filled and its S buffer free, which runs
+//     QK two tiles ahead of the softmax (an item's first two once its Q is in TMEM).
+//   warp 9 (PV): in step k of an item's softmax, forwards the exchange events of that
+//     step to the peer CTA (tile j's partials stored, tile j - 1's peer partials read;
+//     cluster-scope release arrivals, whose memory barrier would otherwise stall the
+//     softmax warps), then PV of tile j - 1 once its P is written; the item's last PV
+//     also signals O final.
+// Separate warps keep a PV (which waits for the softmax) from queueing behind a QK (which
+// waits for the converters), since the converters in turn wait for PV to free a stage.
+template <bool QK>
 __device__ __forceinline__ void mma_warp(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int items,
-                                         uint32_t tmem, int lane) {
+                                         uint32_t tmem, int lane, uint32_t peer) {
   constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTile, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDHalf, false, true);
   // Shared-memory descriptors: a base descriptor per operand plus constant offsets in
-  // its address field (address >> 4, 14 bits; every offset here stays inside the field),
-  // so each UMMA costs one add on the issuing lane.
+  // its address field (address >> 4, 14 bits; every offset here stays inside the field).
+  // The issue loops stay rolled: the tensor core, not the issuing lane, sets their pace,
+  // and small loops keep these warps' code resident in the instruction cache.
   const uint64_t dstage = desc_sw128(smem_u32(smem), 16, 1024);         // K-major B of QK
   const uint64_t dvstage = desc_sw128(smem_u32(smem), kSlab, 1024);     // MN-major B of PV
   const uint64_t dp = desc_sw128(smem_u32(smem + kOffP), 16, 1024);     // A of PV
-  auto issue_qk = [&](int jj) {  // S(jj) = Q K(jj)^T into S buffer jj & 1
-    const uint64_t b = dstage + (uint64_t)(((jj & (kStages - 1)) * kStageBytes) >> 4);
-    const uint32_t d = tmem + kColS + (jj & 1) * kTile;
-#pragma unroll
-    for (int kk = 0; kk < kDHalf / 16; ++kk)
-      umma_ts(d, tmem + kColQ + kk * 8, b + (uint64_t)((((kk >> 2) * kSlab) + (kk & 3) * 32) >> 4), kIdescQK,
-              kk > 0 ? 1u : 0u);
-    umma_commit(&m->sfull[jj & 1]);
-  };
-  auto issue_pv = [&](int jj, bool first) {  // O += P(jj) V(jj), then free the stage and P buffer
-    const uint64_t a = dp + (uint64_t)(((jj & 1) * kPBytes) >> 4);
-    const uint64_t b = dvstage + (uint64_t)(((jj & (kStages - 1)) * kStageBytes) >> 4);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk)
-      umma_ss(tmem + kColO, a + (uint64_t)((kk * 32) >> 4), b + (uint64_t)((kk * 2048) >> 4), kIdescPV,
-              (!first || kk > 0) ? 1u : 0u);
-    umma_commit(&m->kempty[jj & (kStages - 1)]);
-    umma_commit(&m->pvdone[jj & 1]);
-  };
-  auto pv = [&](int jj, bool first, bool last) -> bool {
-    if (!wait_bar_warp(&m->pfull[jj & 1], (jj >> 1) & 1, m)) return false;
+  auto qk = [&](int jj, bool wait_sfree) -> bool {  // S(jj) = Q K(jj)^T into S buffer jj & 1
+    if (!wait_bar_warp<true>(&m->kfull[jj & (kStages - 1)], (jj / kStages) & 1, m)) return false;
+    if (wait_sfree && !wait_bar_warp<true>(&m->sfree[jj & 1], ((jj >> 1) - 1) & 1, m)) return false;
     if (lane == 0) {
       tc_fence_after();
-      issue_pv(jj, first);
+      const uint64_t b = dstage + (uint64_t)(((jj & (kStages - 1)) * kStageBytes) >> 4);
+      const uint32_t d = tmem + kColS + (jj & 1) * kTile;
+#pragma unroll 1
+      for (int kk = 0; kk < kDHalf / 16; ++kk)
+        umma_ts(d, tmem + kColQ + kk * 8, b + (uint64_t)((((kk >> 2) * kSlab) + (kk & 3) * 32) >> 4), kIdescQK,
+                kk > 0 ? 1u : 0u);
+      umma_commit(&m->sfull[jj & 1]);
+    }
+    __syncwarp();
+    return true;
+  };
+  auto pv = [&](int jj, bool first, bool last) -> bool {  // O += P(jj) V(jj), then free the stage and P
+    if (!wait_bar_warp<true>(&m->pfull[jj & 1], (jj >> 1) & 1, m)) return false;
+    if (lane == 0) {
+      tc_fence_after();
+      const uint64_t a = dp + (uint64_t)(((jj & 1) * kPBytes) >> 4);
+      const uint64_t b = dvstage + (uint64_t)(((jj & (kStages - 1)) * kStageBytes) >> 4);
+#pragma unroll 1
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        umma_ss(tmem + kColO, a + (uint64_t)((kk * 32) >> 4), b + (uint64_t)((kk * 2048) >> 4), kIdescPV,
+                (!first || kk > 0) ? 1u : 0u);
+      umma_commit(&m->kempty[jj & (kStages - 1)]);
+      umma_commit(&m->pvdone[jj & 1]);
       if (last) umma_commit(&m->odone);
     }
     __syncwarp();
     return true;
   };
+  auto forward = [&](uint64_t* local, uint32_t parity, uint64_t* remote) -> bool {
+    if (!wait_bar_warp<true>(local, parity, m)) return false;
+    if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(remote), peer));
+    __syncwarp();
+    return true;
+  };
   bool ok = true;
-  int j = 0;    // sequence number of the item's first tile
+  int j0 = 0;   // sequence number of the item's first tile
   int neq = 0;  // items with tiles so far
   for (int w = cid; w < items && ok; w += p.G) {
     const int n = item_of(p, w).n;
     if (n == 0) continue;
-    for (int k = 0; k < n && ok; ++k) {
-      const int jq = j + k;
-      ok = wait_bar_warp(&m->kfull[jq & (kStages - 1)], (jq / kStages) & 1, m);
-      if (ok && k == 0) ok = wait_bar_warp(&m->qready, neq & 1, m);  // Q follows every earlier S load
-      if (ok && k > 0 && jq >= 2) ok = wait_bar_warp(&m->sfree[jq & 1], ((jq >> 1) - 1) & 1, m);
-      if (!ok) break;
-      if (lane == 0) {
-        tc_fence_after();
-        issue_qk(jq);
+    if constexpr (QK) {
+      ok = wait_bar_warp<true>(&m->qready, neq & 1, m);  // the S buffers were freed before Q
+      if (ok) ok = qk(j0, false);
+      if (ok && n > 1) ok = qk(j0 + 1, false);
+      for (int k = 2; k < n && ok; ++k) ok = qk(j0 + k, true);
+    } else {
+      for (int k = 0; k < n && ok; ++k) {
+        const int jj = j0 + k;
+        ok = forward(&m->xsent[jj & 1], (jj >> 1) & 1, &m->xfull[jj & 1]);
+        if (ok && k > 0) ok = forward(&m->xread[(jj - 1) & 1], ((jj - 1) >> 1) & 1, &m->xempty[(jj - 1) & 1]);
+        if (ok && k > 0) ok = pv(jj - 1, k == 1, false);
       }
-      __syncwarp();
-      if (k > 0) ok = pv(jq - 1, k == 1, false);
+      if (ok) ok = forward(&m->xread[(j0 + n - 1) & 1], ((j0 + n - 1) >> 1) & 1, &m->xempty[(j0 + n - 1) & 1]);
+      if (ok) ok = pv(j0 + n - 1, n == 1, true);
     }
-    if (ok) ok = pv(j + n - 1, n == 1, true);
-    j += n;
+    j0 += n;
     ++neq;
   }
   if (!ok && lane == 0) record_abort(m, p.status);
   if (lane == 0) {
-    umma_commit(&m->drain);  // every issued UMMA lands before TMEM is freed
-    mbar_wait_bounded(&m->drain, 0, kWaitLimitNs);
+    umma_commit(&m->drain[QK ? 0 : 1]);  // every UMMA this warp issued lands before TMEM is freed
+    mbar_wait_bounded(&m->drain[QK ? 0 : 1], 0, kWaitLimitNs);
   }
   __syncwarp();
 }
 
-// The loader warp (warp 9, TMA mode): puts the raw tiles in flight in order, four rows
+// The loader warp (warp 10, TMA mode): puts the raw tiles in flight in order, four rows
 // per TMA gather (the CTA's half of every 576-byte data row; masked rows read row 0 and
 // are zeroed by the converters) plus each row's 8-byte scale row, as far ahead as the
 // 3-slot ring allows.  The slots of the next two tiles are prefetched into registers.
@@ -380,7 +425,7 @@ __device__ __forceinline__ void loader_warp(uint8_t* smem, Misc* m, const AttnPa
   int32_t ga1 = load_gidx(pre, lane), gb1 = load_gidx(pre, lane + 32);
   for (int q = 0; iss.valid(); ++q) {
     const int slot = q % kRingSlots;
-    if (q >= kRingSlots && !wait_bar_warp(&m->rawempty[slot], (q / kRingSlots - 1) & 1, m)) {
+    if (q >= kRingSlots && !wait_bar_warp<true>(&m->rawempty[slot], (q / kRingSlots - 1) & 1, m)) {
       if (lane == 0) record_abort(m, p.status);
       break;
     }
@@ -417,7 +462,7 @@ __device__ __forceinline__ void loader_warp(uint8_t* smem, Misc* m, const AttnPa
   __syncwarp();
 }
 
-// The converter warps (10-15, ct = 0..191) of the TMA mode: each raw tile the loader
+// The converter warps (11-15, ct = 0..159) of the TMA mode: each raw tile the loader
 // warp put in flight is dequantised into its stage.
 template <int HALF>
 __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int items, int ct) {
@@ -431,8 +476,8 @@ __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnPa
     uint8_t* stage = smem + s * kStageBytes;
     // A wait that gives up flags the CTA; the converters still run their remaining tile
     // sequence without converting, and every later wait returns at once.
-    bool live = j < kStages || wait_bar(&m->kempty[s], ((j / kStages) - 1) & 1, m);
-    live = live && wait_bar(&m->rawfull[slot], (j / kRingSlots) & 1, m);
+    bool live = j < kStages || wait_bar<true>(&m->kempty[s], ((j / kStages) - 1) & 1, m);
+    live = live && wait_bar<true>(&m->rawfull[slot], (j / kRingSlots) & 1, m);
     if (!live) record_abort(m, p.status);
     live = __all_sync(0xffffffffu, live && !aborted(m));  // warp-uniform: the loop has warp collectives
     if (live) {
@@ -440,38 +485,47 @@ __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnPa
       const uint32_t mk0 = m->maskring[slot][0], mk1 = m->maskring[slot][1];
       auto valid_row = [&](int r) { return (((r < 32 ? mk0 : mk1) >> (r & 31)) & 1u) != 0u; };
       // NoPE: 64 rows x NN pieces; consecutive threads take consecutive pieces of a row.
-      // The pieces are loaded first, then converted on the fast path unless a piece of
-      // the warp needs the exact one.
+      // Pieces are loaded four at a time and converted on the fast path; a batch in which
+      // a piece of the warp needs the exact path (rare) is redone piece by piece.
       constexpr int NI = (kTile * F::NN + kConverters - 1) / kConverters;
-      uint4 v[NI];
-      uint32_t code[NI];
-      bool clean = true;
+      constexpr int NB = 4;
+#pragma unroll 1
+      for (int i0 = 0; i0 < NI; i0 += NB) {
+        uint4 v[NB];
+        uint32_t code[NB];
+        bool clean = true;
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int pc = ct + kConverters * i;
-        const int r = pc / F::NN, k = pc - r * F::NN;
-        v[i] = make_uint4(0, 0, 0, 0);
-        code[i] = 0;
-        if (pc < kTile * F::NN) {
-          v[i] = *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16);
-          code[i] = raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)];
-          clean = clean && code[i] <= 134u && fp8x16_no_nan(v[i]);
+        for (int i = 0; i < NB; ++i) {
+          const int pc = ct + kConverters * (i0 + i);
+          const int r = pc / F::NN, k = pc - r * F::NN;
+          v[i] = make_uint4(0, 0, 0, 0);
+          code[i] = 0;
+          if (i0 + i < NI && pc < kTile * F::NN) {
+            v[i] = *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16);
+            code[i] = raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)];
+            clean = clean && code[i] <= 134u && fp8x16_no_nan(v[i]);
+          }
         }
-      }
-      const bool fast = __all_sync(0xffffffffu, clean);
+        if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int pc = ct + kConverters * i;
-        const int r = pc / F::NN, k = pc - r * F::NN;
-        if (pc < kTile * F::NN) {
-          if (fast)
-            convert_nope<true>(stage, r, k, v[i], code[i], valid_row(r));
-          else
-            convert_nope<false>(stage, r, k, v[i], code[i], valid_row(r));
+          for (int i = 0; i < NB; ++i) {
+            const int pc = ct + kConverters * (i0 + i);
+            const int r = pc / F::NN, k = pc - r * F::NN;
+            if (i0 + i < NI && pc < kTile * F::NN) convert_nope<true>(stage, r, k, v[i], code[i], valid_row(r));
+          }
+        } else {
+#pragma unroll 1
+          for (int i = 0; i < NB; ++i) {
+            const int pc = ct + kConverters * (i0 + i);
+            const int r = pc / F::NN, k = pc - r * F::NN;
+            if (i0 + i < NI && pc < kTile * F::NN)
+              convert_nope<false>(stage, r, k, *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16),
+                                  raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)], valid_row(r));
+          }
         }
       }
       if constexpr (F::NR > 0) {
-#pragma unroll
+#pragma unroll 1
         for (int i = 0; i < (kTile * F::NR + kConverters - 1) / kConverters; ++i) {
           const int pc = ct + kConverters * i;
           if (pc < kTile * F::NR) {
@@ -487,9 +541,9 @@ __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnPa
         m->mask[s][1] = mk1;
       }
     }
-    mbar_arrive(&m->rawempty[slot]);
+    warp_arrive(&m->rawempty[slot]);
     fence_async_smem();
-    mbar_arrive(&m->kfull[s]);
+    warp_arrive(&m->kfull[s]);
     conv.next(p);
   }
 }
@@ -508,7 +562,7 @@ __device__ __forceinline__ void produce_direct(uint8_t* smem, Misc* m, const Att
   for (int j = 0; conv.valid(); ++j) {
     const int s = j & (kStages - 1);
     uint8_t* stage = smem + s * kStageBytes;
-    bool live = j < kStages || wait_bar(&m->kempty[s], ((j / kStages) - 1) & 1, m);
+    bool live = j < kStages || wait_bar<true>(&m->kempty[s], ((j / kStages) - 1) & 1, m);
     if (!live) record_abort(m, p.status);
     live = __all_sync(0xffffffffu, live && !aborted(m));
     auto slot_of = [&](int r) -> int32_t {
@@ -539,7 +593,7 @@ __device__ __forceinline__ void produce_direct(uint8_t* smem, Misc* m, const Att
       }
     }
     fence_async_smem();
-    mbar_arrive(&m->kfull[s]);
+    warp_arrive(&m->kfull[s]);
     conv.next(p);
   }
 }
@@ -579,26 +633,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&m->kfull[s], kConverters);
+      mbar_init(&m->kfull[s], kConverters / 32);
       mbar_init(&m->kempty[s], 1);
     }
     for (int r = 0; r < kRingSlots; ++r) {
       mbar_init(&m->rawfull[r], 1 + 32);  // the loader's expect-tx + its 32 lanes' scale copies
-      mbar_init(&m->rawempty[r], kConverters);
+      mbar_init(&m->rawempty[r], kConverters / 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&m->sfull[b], 1);
-      mbar_init(&m->sfree[b], kSoftmaxThreads);
-      mbar_init(&m->pfull[b], kSoftmaxThreads);
+      mbar_init(&m->sfree[b], kSoftmaxThreads / 32);
+      mbar_init(&m->pfull[b], kSoftmaxThreads / 32);
       mbar_init(&m->pvdone[b], 1);
-      mbar_init(&m->xfull[b], kSoftmaxThreads);
-      mbar_init(&m->xempty[b], kSoftmaxThreads);
+      mbar_init(&m->xsent[b], kSoftmaxThreads / 32);
+      mbar_init(&m->xread[b], kSoftmaxThreads / 32);
+      mbar_init(&m->xfull[b], 1);
+      mbar_init(&m->xempty[b], 1);
     }
     mbar_init(&m->odone, 1);
-    mbar_init(&m->drain, 1);
-    mbar_init(&m->sgrp, kSoftmaxThreads);
-    mbar_init(&m->qready, kSoftmaxThreads);
-    for (int i = 0; i < 4; ++i) mbar_init(&m->hpair[i], 64);
+    mbar_init(&m->drain[0], 1);
+    mbar_init(&m->drain[1], 1);
+    mbar_init(&m->sgrp, kSoftmaxThreads / 32);
+    mbar_init(&m->qready, kSoftmaxThreads / 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&m->hpair[i], 2);
     m->abort = 0;
     fence_mbar_init();
   }
@@ -659,7 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st32(tmem + lane_base + kColQ + hc * 64 + 32, r[1]);
         tmem_wait_st();
         tc_fence_before();
-        if (n > 0) mbar_arrive(&m->qready);  // the issuer may start QK of the item's first tile
+        if (n > 0) warp_arrive(&m->qready);  // the issuer may start QK of the item's first tile
       }
 
       float m_ref = -INFINITY;  // reference max (log2 domain) the weights are taken against
@@ -694,20 +751,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           // S is in registers: QK of tile j + 2 may reuse the buffer.
           tc_fence_before();
-          mbar_arrive(&m->sfree[j & 1]);
+          warp_arrive(&m->sfree[j & 1]);
           // Send: the peer's buffer j & 1 is free once the peer has read tile j - 2.
           if (j >= 2 && !(ok = wait_bar_warp(&m->xempty[j & 1], ((j >> 1) - 1) & 1, m, true))) break;
           float* dst = xbuf(peer, j & 1);
 #pragma unroll
           for (int i = 0; i < kCols / 4; ++i)
             st_global_f4(dst + i * (kSoftmaxThreads * 4), xc[4 * i], xc[4 * i + 1], xc[4 * i + 2], xc[4 * i + 3]);
-          // (the release that publishes them comes after tile jl is finished, by which
-          // time the stores have reached L2 and the release does not stall)
+          warp_arrive(&m->xsent[j & 1]);  // the PV warp publishes them to the peer
         }
         if (k > 0) {
           // Finish tile jl: the 512-wide scores in log2 units.
 #pragma unroll
           for (int i = 0; i < kCols; ++i) rv[i] = (xp[i] + rv[i]) * sl2;
+          warp_arrive(&m->xread[jl & 1]);  // the peer's partials of tile jl are consumed
           // The stage's valid-row mask (published by the converters before kfull).
           const int s = jl & (kStages - 1);
           if (!(ok = wait_bar_warp(&m->kfull[s], (jl / kStages) & 1, m))) break;
@@ -726,7 +783,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           // Both threads of head h agree on the tile max and so on m_ref.
           m->red[jl & 1][hc][h] = lmax;
-          mbar_arrive(&m->hpair[warp & 3]);
+          warp_arrive(&m->hpair[warp & 3]);
           if (!(ok = wait_bar_warp(&m->hpair[warp & 3], jl & 1, m))) break;
           const float tmax = fmaxf(lmax, m->red[jl & 1][hc ^ 1][h]);
           float alpha = 1.f;
@@ -774,12 +831,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           fence_async_smem();
           tc_fence_before();
-          mbar_arrive(&m->pfull[jl & 1]);
+          warp_arrive(&m->pfull[jl & 1]);
           ok = !aborted(m);
           if (!(ok = __all_sync(0xffffffffu, ok))) break;
-          mbar_arrive_cluster(mapa(smem_u32(&m->xempty[jl & 1]), peer));  // my buffer jl & 1 is read
         }
-        if (k < n) mbar_arrive_cluster(mapa(smem_u32(&m->xfull[j & 1]), peer));  // tile j's partials
         if (k < n) {
 #pragma unroll
           for (int i = 0; i < kCols; ++i) xp[i] = xc[i];
@@ -794,7 +849,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // Epilogue: head h, local dims [128 hc, 128 hc + 128) of this CTA's 256.
       tc_fence_after();
       m->red[0][hc][h] = l_run;  // every use of red[][] by the tile loop is over (odone)
-      mbar_arrive(&m->sgrp);
+      warp_arrive(&m->sgrp);
       if (!(ok = wait_bar_warp(&m->sgrp, sgrp_phase, m))) break;
       sgrp_phase ^= 1u;
       const float l_tot = l_run + m->red[0][hc ^ 1][h];
@@ -865,7 +920,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // O, Q and red[] are reused by the next item: every thread's reads end here.
       tc_fence_before();
-      mbar_arrive(&m->sgrp);
+      warp_arrive(&m->sgrp);
       if (!(ok = wait_bar_warp(&m->sgrp, sgrp_phase, m))) break;
       sgrp_phase ^= 1u;
       tc_fence_after();
@@ -876,24 +931,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ gather + dequant
     const int pt = tid - kSoftmaxThreads;
     if (pt < 32) {
-      mma_warp(smem, m, p, cid, items, tmem, pt);
+      mma_warp<true>(smem, m, p, cid, items, tmem, pt, peer);
     } else if (pt < 64) {
+      mma_warp<false>(smem, m, p, cid, items, tmem, pt - 32, peer);
+    } else if (pt < 96) {
       if constexpr (TMA) {
         if (half == 0)
-          loader_warp<0>(smem, m, p, &kp.map[0], cid, items, pt - 32);
+          loader_warp<0>(smem, m, p, &kp.map[0], cid, items, pt - 64);
         else
-          loader_warp<1>(smem, m, p, &kp.map[1], cid, items, pt - 32);
+          loader_warp<1>(smem, m, p, &kp.map[1], cid, items, pt - 64);
       }
     } else if constexpr (TMA) {
       if (half == 0)
-        produce_tma<0>(smem, m, p, cid, items, pt - 64);
+        produce_tma<0>(smem, m, p, cid, items, pt - 96);
       else
-        produce_tma<1>(smem, m, p, cid, items, pt - 64);
+        produce_tma<1>(smem, m, p, cid, items, pt - 96);
     } else {
       if (half == 0)
-        produce_direct<0>(smem, m, p, cid, items, pt - 64);
+        produce_direct<0>(smem, m, p, cid, items, pt - 96);
       else
-        produce_direct<1>(smem, m, p, cid, items, pt - 64);
+        produce_direct<1>(smem, m, p, cid, items, pt - 96);
     }
   }
 
