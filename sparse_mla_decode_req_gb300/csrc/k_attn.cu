@@ -116,7 +116,7 @@ struct Misc {
   uint64_t drain[2];         // the MMA warps' self-drain before TMEM is freed
   uint64_t sgrp;             // softmax-group rendezvous (8 warps per use)
   uint64_t qready;           // softmax -> issuer: an item's Q is in TMEM (8 warps)
-  uint64_t rawfull[kRingSlots];   // raw tile landed (loader expect-tx + 32 scale-copy arrivals)
+  uint64_t rawfull[kRingSlots];   // raw tile landed (loader expect-tx arrival + codes arrival + TMA bytes)
   uint64_t rawempty[kRingSlots];  // raw tile converted (one arrival per converter warp)
   uint64_t hpair[4];         // warps w and w+4 (the two threads of heads 32w..32w+31): 2
   uint32_t tmem_base;
@@ -129,8 +129,6 @@ struct Misc {
 // (checked at run time), so no slack is reserved.
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-__device__ __align__(16) uint8_t g_zero_row[320];  // source of the copies of masked rows
 
 __device__ __forceinline__ float ex2(float x) { return fast_exp2(x); }
 
@@ -192,15 +190,8 @@ __device__ __forceinline__ uint32_t stage_off(uint32_t row, uint32_t d0) {
   return (d0 >> 6) * kSlab + sw128_off(row, (d0 & 63) >> 3);
 }
 
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued so far has landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void st_global_f4(float* p, float a, float b, float c, float d) {
   asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
@@ -274,20 +265,15 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 }
 
 // Dequantises the 16-byte NoPE piece `k` of a raw row (scale code from its scale row)
-// into the stage, or zeros when the row is masked.
-// (elements in the (d0, d2, d1, d3) order of dequant16_perm_*; `fast` must be warp-uniform
-// and true only when no piece of the warp holds a NaN byte or a code above 134).
-template <bool FAST>
+// into the stage on the exact path (any bytes, any code), or zeros when the row is masked;
+// elements in the (d0, d2, d1, d3) order of dequant16_perm_*.
 __device__ __forceinline__ void convert_nope(uint8_t* stage, int srow, int k, uint4 raw, uint32_t code, bool valid) {
   uint4 lo, hi;
   if (!valid) {
     raw = make_uint4(0, 0, 0, 0);
     code = 0;
   }
-  if constexpr (FAST)
-    dequant16_perm_fast(raw, code, lo, hi);
-  else
-    dequant16_perm_exact(raw, code, lo, hi);
+  dequant16_perm_exact(raw, code, lo, hi);
   *reinterpret_cast<uint4*>(stage + stage_off(srow, k * 16)) = lo;
   *reinterpret_cast<uint4*>(stage + stage_off(srow, k * 16 + 8)) = hi;
 }
@@ -391,8 +377,10 @@ __device__ __forceinline__ void mma_warp(uint8_t* smem, Misc* m, const AttnParam
 
 // The loader warp (warp 10, TMA mode): puts the raw tiles in flight in order, four rows
 // per TMA gather (the CTA's half of every 576-byte data row; masked rows read row 0 and
-// are zeroed by the converters) plus each row's 8-byte scale row, as far ahead as the
-// 3-slot ring allows.  The slots of the next two tiles are prefetched into registers.
+// are zeroed by the converters), as far ahead as the 3-slot ring allows.  The four scale
+// codes of the half (one 32-bit word of each row's 8-byte scale row) are read with plain
+// loads one tile ahead and stored into the slot with the tile; the slots of the next two
+// tiles are prefetched into registers.
 template <int HALF>
 __device__ __forceinline__ void loader_warp(uint8_t* smem, Misc* m, const AttnParams& p, const CUtensorMap* map,
                                             int cid, int items, int lane) {
@@ -411,31 +399,35 @@ __device__ __forceinline__ void loader_warp(uint8_t* smem, Misc* m, const AttnPa
     slot_page_off(cv, sl, page, off);
     return page * rows_per_page16 + off * (kDataBytes / 16);
   };
-  auto scale_row = [&](int32_t sl) -> const uint8_t* {
-    if (sl < 0) return g_zero_row;
+  auto codes = [&](int32_t sl) -> uint32_t {  // the half's four scale codes of slot sl (0 if masked)
+    if (sl < 0) return 0u;
     int32_t page, off;
     slot_page_off(cv, sl, page, off);
-    return cv.base + (int64_t)page * cv.page_bytes + cv.scale_start + (int64_t)off * kScaleBytes;
+    return ldg_nc_u32(cv.base + (int64_t)page * cv.page_bytes + cv.scale_start + (int64_t)off * kScaleBytes +
+                      F::CODE0);
   };
   TileCursor iss, pre;
   iss.init(p, cid, p.G, items);
   pre = iss;
   int32_t ga0 = load_gidx(pre, lane), gb0 = load_gidx(pre, lane + 32);
+  uint32_t ca0 = codes(ga0), cb0 = codes(gb0);
   pre.next(p);
   int32_t ga1 = load_gidx(pre, lane), gb1 = load_gidx(pre, lane + 32);
+  int issued = 0;
   for (int q = 0; iss.valid(); ++q) {
     const int slot = q % kRingSlots;
     if (q >= kRingSlots && !wait_bar_warp<true>(&m->rawempty[slot], (q / kRingSlots - 1) & 1, m)) {
       if (lane == 0) record_abort(m, p.status);
       break;
     }
-    const uint32_t base = smem_u32(ring + slot * F::SLOT);
+    uint8_t* sbase = ring + slot * F::SLOT;
+    const uint32_t base = smem_u32(sbase);
     const bool va = ga0 >= 0, vb = gb0 >= 0;
     const uint32_t ba = __ballot_sync(0xffffffffu, va), bb = __ballot_sync(0xffffffffu, vb);
     if (lane == 0) {
       m->maskring[slot][0] = ba;
       m->maskring[slot][1] = bb;
-      mbar_arrive_expect_tx(&m->rawfull[slot], kTile * F::DATA);  // releases maskring
+      mbar_arrive_expect_tx(&m->rawfull[slot], kTile * F::DATA);
     }
     __syncwarp();
     const int32_t ya = va ? row16(ga0) : 0, yb = vb ? row16(gb0) : 0;  // masked rows read row 0
@@ -448,17 +440,25 @@ __device__ __forceinline__ void loader_warp(uint8_t* smem, Misc* m, const AttnPa
     }
     if (lane < 16)
       tma_gather4(base + 4 * lane * F::DATA, map, F::BYTE0 / 2, y[0], y[1], y[2], y[3], &m->rawfull[slot]);
-    cp_async8(base + F::SCALES + lane * 8, scale_row(ga0));
-    cp_async8(base + F::SCALES + (lane + 32) * 8, scale_row(gb0));
-    cp_async_arrive(&m->rawfull[slot]);
+    const uint32_t ca1 = codes(ga1), cb1 = codes(gb1);  // next tile's codes, in flight meanwhile
+    *reinterpret_cast<uint32_t*>(sbase + F::SCALES + lane * 8 + F::CODE0) = ca0;
+    *reinterpret_cast<uint32_t*>(sbase + F::SCALES + (lane + 32) * 8 + F::CODE0) = cb0;
+    warp_arrive(&m->rawfull[slot]);  // releases maskring and the codes
     iss.next(p);
     ga0 = ga1;
     gb0 = gb1;
+    ca0 = ca1;
+    cb0 = cb1;
     pre.next(p);
     ga1 = load_gidx(pre, lane);
     gb1 = load_gidx(pre, lane + 32);
+    ++issued;
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after the CTA is gone
+  // No gather may land after the CTA is gone (the converters skip their waits once the
+  // CTA has aborted): wait, bounded, for the last tiles put in flight.
+  if (lane == 0)
+    for (int t = issued > kRingSlots ? issued - kRingSlots : 0; t < issued; ++t)
+      (void)mbar_wait_bounded(&m->rawfull[t % kRingSlots], (t / kRingSlots) & 1, kWaitLimitNs);
   __syncwarp();
 }
 
@@ -485,15 +485,16 @@ __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnPa
       const uint32_t mk0 = m->maskring[slot][0], mk1 = m->maskring[slot][1];
       auto valid_row = [&](int r) { return (((r < 32 ? mk0 : mk1) >> (r & 31)) & 1u) != 0u; };
       // NoPE: 64 rows x NN pieces; consecutive threads take consecutive pieces of a row.
-      // Pieces are loaded four at a time and converted on the fast path; a batch in which
-      // a piece of the warp needs the exact path (rare) is redone piece by piece.
+      // Pieces are loaded four at a time and converted on the fast path (exact for any
+      // bytes when the scale code is at most 134); a thread redoes its pieces with larger
+      // codes (rare) on the exact path afterwards, overwriting the fast result.
       constexpr int NI = (kTile * F::NN + kConverters - 1) / kConverters;
       constexpr int NB = 4;
 #pragma unroll 1
       for (int i0 = 0; i0 < NI; i0 += NB) {
         uint4 v[NB];
         uint32_t code[NB];
-        bool clean = true;
+        uint32_t redo = 0;
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
           const int pc = ct + kConverters * (i0 + i);
@@ -503,24 +504,30 @@ __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnPa
           if (i0 + i < NI && pc < kTile * F::NN) {
             v[i] = *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16);
             code[i] = raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)];
-            clean = clean && code[i] <= 134u && fp8x16_no_nan(v[i]);
           }
         }
-        if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll
-          for (int i = 0; i < NB; ++i) {
-            const int pc = ct + kConverters * (i0 + i);
-            const int r = pc / F::NN, k = pc - r * F::NN;
-            if (i0 + i < NI && pc < kTile * F::NN) convert_nope<true>(stage, r, k, v[i], code[i], valid_row(r));
+        for (int i = 0; i < NB; ++i) {
+          const int pc = ct + kConverters * (i0 + i);
+          const int r = pc / F::NN, k = pc - r * F::NN;
+          if (i0 + i < NI && pc < kTile * F::NN) {
+            const bool valid = valid_row(r);
+            uint4 lo, hi;
+            dequant16_perm_nz(valid ? v[i] : make_uint4(0, 0, 0, 0), valid ? code[i] : 0u, lo, hi);
+            *reinterpret_cast<uint4*>(stage + stage_off(r, k * 16)) = lo;
+            *reinterpret_cast<uint4*>(stage + stage_off(r, k * 16 + 8)) = hi;
+            redo |= (valid && code[i] > 134u) ? (1u << i) : 0u;
           }
-        } else {
+        }
+        if (redo != 0u) {
 #pragma unroll 1
           for (int i = 0; i < NB; ++i) {
-            const int pc = ct + kConverters * (i0 + i);
-            const int r = pc / F::NN, k = pc - r * F::NN;
-            if (i0 + i < NI && pc < kTile * F::NN)
-              convert_nope<false>(stage, r, k, *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16),
-                                  raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)], valid_row(r));
+            if ((redo >> i) & 1u) {
+              const int pc = ct + kConverters * (i0 + i);
+              const int r = pc / F::NN, k = pc - r * F::NN;
+              convert_nope(stage, r, k, *reinterpret_cast<const uint4*>(raw + r * F::DATA + k * 16),
+                                  raw[F::SCALES + r * 8 + F::CODE0 + (k >> 2)], true);
+            }
           }
         }
       }
@@ -583,7 +590,7 @@ __device__ __forceinline__ void produce_direct(uint8_t* smem, Misc* m, const Att
           if (k < F::NN) code = ldg_nc_u8(row_scales(cv, g) + F::CODE0 + (k >> 2));
         }
         if (k < F::NN)
-          convert_nope<false>(stage, r, k, v, code, g >= 0);
+          convert_nope(stage, r, k, v, code, g >= 0);
         else
           *reinterpret_cast<uint4*>(stage + stage_off(r, 192 + (k - F::NN) * 8)) = scrub_bf16x8(v);
       }
@@ -637,7 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&m->kempty[s], 1);
     }
     for (int r = 0; r < kRingSlots; ++r) {
-      mbar_init(&m->rawfull[r], 1 + 32);  // the loader's expect-tx + its 32 lanes' scale copies
+      mbar_init(&m->rawfull[r], 2);  // the loader's expect-tx arrival, then its arrival after the codes
       mbar_init(&m->rawempty[r], kConverters / 32);
     }
     for (int b = 0; b < 2; ++b) {

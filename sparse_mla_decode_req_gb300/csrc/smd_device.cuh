@@ -190,6 +190,12 @@ __device__ __forceinline__ void dequant16_perm_fast(uint4 in, uint32_t code, uin
   lo = make_uint4(r[0], r[1], r[2], r[3]);
   hi = make_uint4(r[4], r[5], r[6], r[7]);
 }
+// The fast path for any bytes: NaN encodings are zeroed first (as the exact path does),
+// so it is exact whenever code <= 134.
+__device__ __forceinline__ void dequant16_perm_nz(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
+  dequant16_perm_fast(make_uint4(zero_fp8_nans(in.x), zero_fp8_nans(in.y), zero_fp8_nans(in.z), zero_fp8_nans(in.w)),
+                      code, lo, hi);
+}
 // Any input (NaN bytes, large or NaN codes): the exact path, then the same reordering.
 __device__ __forceinline__ void dequant16_perm_exact(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
   dequant16_fast(in, code, lo, hi);
@@ -234,6 +240,11 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 __device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
   uint2 v;
   asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ uint32_t ldg_nc_u8(const void* p) {
