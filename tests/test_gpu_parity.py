@@ -272,3 +272,28 @@ def test_staged_calls_match_oracle(ns):
     assert_out_close(out, ro, f"staged splits {ns}")
     assert_lse_close(lse, rl, f"staged splits {ns}")
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("P", [64, 2, 3])
+def test_decode_index_edge_cases(P):
+    """The whole decode step over request ids, blocks and pages out of range, negative
+    indices and strided index rows, against the oracle."""
+    gen = torch.Generator().manual_seed(100 + P)
+    R, B, pages, T, K, W, H = 5, 9, 20, 7, 50, 13, 16
+    bt = torch.randint(-3, pages + 4, (R, B + 3), generator=gen, dtype=torch.int32)
+    req = torch.randint(-1, R + 2, (T,), generator=gen, dtype=torch.int32)
+    topk = torch.randint(-3, B * P + 5, (T, K + 6), generator=gen, dtype=torch.int32)
+    swa = torch.randint(-3, B * P + 5, (T, W), generator=gen, dtype=torch.int32)
+    cache = synth.make_cache(pages, P, seed=7 + P, device="cuda")
+    q = (torch.randn(T, H, 512, generator=gen) * 0.5).to(torch.bfloat16)
+    sink = torch.randn(H, generator=gen)
+    scale = 1.0 / math.sqrt(512)
+    btv, topv = bt[:, :B], topk[:, 2:2 + K]
+    for ns in (1, -3):
+        out, lse = api.sparse_mla_decode(q.cuda(), cache, bt.cuda()[:, :B], req.cuda(), topk.cuda()[:, 2:2 + K],
+                                         swa.cuda(), sink.cuda(), scale, num_splits=ns, block_size=P)
+        torch.cuda.synchronize()
+        ro, rl = oracle.sparse_mla_decode(bf16_to_f64(q), cache.cpu().numpy(), btv.numpy(), req.numpy(),
+                                          topv.numpy(), swa.numpy(), sink.double().numpy(), scale, P)
+        assert_out_close(out, ro, f"edge P={P} splits {ns}")
+        assert_lse_close(lse, rl, f"edge P={P} splits {ns}")
