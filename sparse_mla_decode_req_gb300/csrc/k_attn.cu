@@ -623,6 +623,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sP = smem + kOffP;
   Misc* m = reinterpret_cast<Misc*>(smem + kOffMisc);
 
+  // Launched as a programmatic dependent of the previous kernel in the stream: only the
+  // launch itself overlaps that kernel; everything here waits for its completion.  (No
+  // early trigger for the next kernel: a split combine launched early would pack its
+  // blocks onto the few SMs this grid leaves free; launched at this grid's exit it
+  // spreads over the whole GPU.)
+  grid_dep_wait();
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const uint32_t half = cluster_rank();   // == blockIdx.x & 1
@@ -1040,12 +1046,17 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done[tma][dev] = true;
   }
-  const dim3 grid(2 * p.G, 1);
-  if (tma)
-    attn_pair_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(kp);
-  else
-    attn_pair_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(kp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.G, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return tma ? cudaLaunchKernelEx(&cfg, attn_pair_kernel<true>, kp) : cudaLaunchKernelEx(&cfg, attn_pair_kernel<false>, kp);
 }
 
 }  // namespace smd

@@ -17,6 +17,7 @@
 namespace smd {
 
 __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
+  grid_dep_wait();  // launched as a programmatic dependent of the attention kernel
   const int64_t pair = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // t * H + h
   const int lane = threadIdx.x & 31;
   if (pair >= (int64_t)p.T * p.H) return;
@@ -76,8 +77,16 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t pairs = (int64_t)p.T * p.H;
   if (pairs == 0) return cudaSuccess;
-  lse_combine_kernel<<<(unsigned)((pairs + 7) / 8), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((pairs + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lse_combine_kernel, p);
 }
 
 }  // namespace smd
