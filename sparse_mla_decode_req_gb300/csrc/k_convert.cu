@@ -18,6 +18,7 @@
 namespace smd {
 
 __global__ void __launch_bounds__(256) convert_kernel(ConvertParams p) {
+  grid_dep_wait();  // launched as a programmatic dependent of the previous kernel
   const int32_t t = blockIdx.y;
   const int32_t N = p.K + p.W;
   if (p.status != nullptr && t == 0 && blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0u;
@@ -44,9 +45,16 @@ cudaError_t launch_convert(const ConvertParams& p, cudaStream_t s) {
     if (p.status != nullptr) return cudaMemsetAsync(p.status, 0, sizeof(uint32_t), s);
     return cudaSuccess;
   }
-  dim3 grid((N + 255) / 256, p.T);
-  convert_kernel<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((N + 255) / 256, p.T, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, convert_kernel, p);
 }
 
 }  // namespace smd
