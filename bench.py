@@ -143,6 +143,27 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_seed(config: int, rank: int) -> int:
+    """Each replica draws its own inputs (same shapes, different values)."""
+    from sparse_mla_decode_req_gb300 import synth
+    return synth.SEED_BASE + config + 1000 * rank
+
+
+def max_over_ranks(pg, seconds: float, device) -> float:
+    """The slowest replica's time (the job finishes when the last rank does)."""
+    if pg is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(rows_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: every replica processes rows_per_step per step."""
+    return rows_per_step * steps * world / seconds
+
+
 def cpu_oracle_rate(inp, seconds: float, max_steps: int | None = None):
     """Time the float64 oracle on whole tokens of the workload (cycling) for ~`seconds`."""
     import numpy as np
@@ -224,7 +245,7 @@ def main(argv=None):
         pg = dist
     lib = api.load()
     w = synth.WORKLOADS[args.config]
-    seed = synth.SEED_BASE + args.config + 1000 * rank
+    seed = rank_seed(args.config, rank)
     inp = synth.make_inputs(w, seed=seed, device=dev)
     T, H, N = w.num_tokens, w.num_heads, w.n_entries
     rows_per_step = inp.n_valid
@@ -307,13 +328,9 @@ def main(argv=None):
     attn_ms = [e[1].elapsed_time(e[2]) for e in evk]
     conv_ms = [e[0].elapsed_time(e[1]) for e in evk]
     comb_ms = [e[2].elapsed_time(e[3]) for e in evk]
-    total_s = sum(step_ms) / 1e3
-    if pg is not None:
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(pg, sum(step_ms) / 1e3, dev)
     assert int(status.item()) == 0, "a kernel's bounded wait gave up during the benchmark"
-    value = rows_per_step * K * world / total_s
+    value = job_rate(rows_per_step, K, world, total_s)
     ms_per_step = total_s / K * 1e3
 
     peaks, src = load_peaks()
@@ -325,11 +342,8 @@ def main(argv=None):
     # end to end through the public call with host buffers: h2d of the step's inputs,
     # decode, d2h of out + lse, per step
     e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step)
-    if pg is not None:
-        t = torch.tensor([e2e["seconds"]], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e["seconds"] = float(t.item())
-    e2e_val = rows_per_step * e2e["steps"] * world / e2e["seconds"]
+    e2e["seconds"] = max_over_ranks(pg, e2e["seconds"], dev)
+    e2e_val = job_rate(rows_per_step, e2e["steps"], world, e2e["seconds"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
