@@ -377,18 +377,30 @@ def main(argv=None):
     return 0
 
 
-def load_traffic(name: str):
-    """DRAM bytes per attention launch from a committed ncu summary, if the kernel is unchanged."""
+def kernel_code_hash(path: str) -> str:
+    """Hash of a CUDA source with // comments and blank lines removed: a comment edit
+    leaves the compiled kernel, and so a traffic capture of it, valid."""
     import hashlib
+    import re
+    lines = []
+    with open(path) as f:
+        for line in f:
+            code = re.sub(r"//.*", "", line).rstrip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
+def load_traffic(name: str):
+    """DRAM bytes per attention launch from a committed ncu summary, if the kernel code is
+    unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "attn_traffic.json")
     src = os.path.join(ROOT, "sparse_mla_decode_req_gb300", "csrc", "k_attn.cu")
     try:
         with open(path) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
         e = d.get(name)
-        if e and e.get("k_attn_sha") == sha:
+        if e and e.get("k_attn_code_hash") == kernel_code_hash(src):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass

@@ -31,8 +31,8 @@
 //     buffer j&1 (warp 8), and O_c += P(j) V_c(j) (M128 N256 K64, the stage read
 //     MN-major; warp 9, which also forwards the exchange events to the peer CTA).
 //   warp 10, the loader: puts each tile's raw rows in flight with TMA row gathers (four
-//     rows per gather, the CTA's half of every 576-byte data row) and 8-byte scale-row
-//     copies into the raw ring.
+//     rows per gather, the CTA's half of every 576-byte data row) into the raw ring, with
+//     each row's four scale codes of the half (read one tile ahead).
 //   warps 11-15, the converters: dequantise each raw tile into its stage.
 //   warps 0-7, softmax + epilogue: thread (h, hc) owns head h (TMEM lane h) and score
 //     columns [32 hc, 32 hc + 32) of every tile.
@@ -45,8 +45,10 @@
 // and hands it to PV).  The running max only moves when it grows by more than 2^8, so O
 // is rarely rescaled.
 //
-// Every wait is bounded; a wait that gives up records bit 0 in the status word and the
-// CTA winds down (draining its UMMAs, freeing TMEM).
+// The kernel is launched as a programmatic dependent of the previous kernel in the
+// stream and waits for it at entry.  Every wait is bounded; a wait that gives up records
+// bit 0 in the status word and the CTA winds down (draining its UMMAs and gathers,
+// freeing TMEM).
 #include <cuda.h>
 
 #include "smd_device.cuh"
