@@ -297,3 +297,39 @@ def test_decode_index_edge_cases(P):
                                           topv.numpy(), swa.numpy(), sink.double().numpy(), scale, P)
         assert_out_close(out, ro, f"edge P={P} splits {ns}")
         assert_lse_close(lse, rl, f"edge P={P} splits {ns}")
+
+
+@pytest.mark.parametrize("ns", [1, -3])
+def test_decode_replays_in_a_cuda_graph(ns):
+    """The decode call captured once in a CUDA graph (its split count depends on shapes
+    only) and replayed over two input sets copied into the captured buffers."""
+    w = synth.small_workload(num_tokens=4, num_heads=64, topk=200, swa=40, ctx=700, n_invalid=5)
+    sets = [synth.make_inputs(w, seed=31 + i, device="cuda") for i in range(2)]
+    a = sets[0]
+    st = {k: getattr(a, k).clone() for k in ("q", "kv_cache", "block_table", "req_id", "topk_idx", "swa_idx", "sink")}
+    dims = api.make_dims(st["q"], st["kv_cache"], st["block_table"], st["req_id"], st["topk_idx"], st["swa_idx"])
+    ws = torch.empty(api.workspace_size(dims, ns, 0), dtype=torch.uint8, device="cuda")
+    out = torch.empty(w.num_tokens, w.num_heads, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.num_tokens, w.num_heads, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call():
+        api.sparse_mla_decode(st["q"], st["kv_cache"], st["block_table"], st["req_id"], st["topk_idx"],
+                              st["swa_idx"], st["sink"], a.scale, out=out, lse=lse, num_splits=ns, workspace=ws,
+                              stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()  # first call outside the capture (one-time per-device setup)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    for inp in (sets[1], sets[0]):
+        for k, t in st.items():
+            t.copy_(getattr(inp, k))
+        g.replay()
+        torch.cuda.synchronize()
+        ro, rl = oracle_decode(inp)
+        assert_out_close(out, ro, f"graph replay splits {ns}")
+        assert_lse_close(lse, rl, f"graph replay splits {ns}")
+        assert api.read_status(ws) == 0
