@@ -695,6 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int hc = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = p.scale * kLog2e;
+    const bool pad_warp = (warp & 3) * 32 >= p.H;  // all 32 heads of this warp are padding
     // Exchange buffers (CTA `rank`'s incoming partials) are recomputed at each use (kernel
     // parameters live in the constant bank), which keeps them out of the register budget.
     auto xbuf = [&](uint32_t rank, int b) {
@@ -740,6 +741,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // Step k loads and sends tile j (k < n), then finishes tile j - 1 (k > 0).
       for (int k = 0; k <= n; ++k) {
         const int jl = j - 1;
+        if (pad_warp) {
+          // Heads past H are zero padding whose rows nobody reads: keep only the barrier
+          // protocol, each arrival after a wait that orders it behind the same barrier's
+          // previous phase (sfull(j) follows sfree of tile j - 2; xempty(j) follows xsent
+          // of tile j - 2; pvdone of tile jl - 2 follows every xread and pfull of it).
+          if (k < n) {
+            if (!(ok = wait_bar_warp(&m->sfull[j & 1], (j >> 1) & 1, m))) break;
+            warp_arrive(&m->sfree[j & 1]);
+            if (j >= 2 && !(ok = wait_bar_warp(&m->xempty[j & 1], ((j >> 1) - 1) & 1, m, true))) break;
+            warp_arrive(&m->xsent[j & 1]);
+          }
+          if (k > 0) {
+            if (jl >= 2 && !(ok = wait_bar_warp(&m->pvdone[jl & 1], ((jl >> 1) - 1) & 1, m))) break;
+            warp_arrive(&m->xread[jl & 1]);
+            warp_arrive(&m->pfull[jl & 1]);
+            if (!(ok = __all_sync(0xffffffffu, !aborted(m)))) break;
+          }
+          if (k < n) ++j;
+          continue;
+        }
         float rv[kCols];  // the peer's partials of tile jl
         float xc[kCols];  // this CTA's partials of tile j
         if (k > 0) {  // start reading the peer's partials of tile jl; they are used below
