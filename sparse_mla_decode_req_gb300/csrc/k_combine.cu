@@ -7,18 +7,26 @@
 // with the -inf guard of SGLang PR #26208 report, "评论区精华" (an empty split has
 // lse_s = -inf and weight 0; no terms at all gives out = 0, lse = -inf).
 //
-// One warp per (token, head).  Lane s < S holds lse_s, so the max and the weight sum
-// are two butterfly reductions; each lane then owns 16 of the 512 output dims and
-// streams the S partial rows with 16-byte loads (a warp reads 2 KB contiguous per
-// split) and writes 32 contiguous bytes of bf16.
+// WPP warps per (token, head) (1, 2 or 4), each owning 512 / WPP output dims.  Lane
+// s < S holds lse_s, so the max and the weight sum are two butterfly reductions (each
+// warp does them); each lane then streams its 16 / WPP consecutive dims of the S
+// partial rows with 16-byte loads (a warp reads 2048 / WPP contiguous bytes per split)
+// and writes them as bf16.
+// The host takes WPP = 4 when the step has few (token, head) pairs, so that enough
+// loads are in flight, and fewer warps per pair once the grid would pass one wave.
 #include "smd_device.cuh"
 #include "smd_internal.h"
 
 namespace smd {
 
+template <int WPP>
 __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
+  constexpr int kNv = 4 / WPP;                 // float4 per lane and split
+  constexpr int kDimsPerWarp = kLatent / WPP;  // 128 * kNv
   grid_dep_wait();  // launched as a programmatic dependent of the attention kernel
-  const int64_t pair = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // t * H + h
+  const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t pair = gw / WPP;  // t * H + h
+  const int part = (int)(gw - pair * WPP);
   const int lane = threadIdx.x & 31;
   if (pair >= (int64_t)p.T * p.H) return;
   const int32_t t = (int32_t)(pair / p.H);
@@ -34,11 +42,14 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   M = fmaxf(M, sink);
 
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + pair * (kLatent * 2)) + lane * 2;
+  // This lane's dims: 4 kNv consecutive ones from d0.
+  const int d0 = part * kDimsPerWarp + lane * 4 * kNv;
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + (pair * kLatent + d0) * 2);
+  const bool writes_lse = p.lse != nullptr && part == 0 && lane == 0;
   if (M == ninf) {  // no entries and no sink
-    dst[0] = make_uint4(0, 0, 0, 0);
-    dst[1] = make_uint4(0, 0, 0, 0);
-    if (p.lse != nullptr && lane == 0) p.lse[pair] = ninf;
+#pragma unroll
+    for (int i = 0; i < kNv; ++i) dst[i] = make_uint2(0, 0);
+    if (writes_lse) p.lse[pair] = ninf;
     return;
   }
   const float w_mine = l_mine == ninf ? 0.f : exp2f((l_mine - M) * kLog2e);
@@ -48,37 +59,47 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
   den += sink == ninf ? 0.f : exp2f((sink - M) * kLog2e);
   const float inv = 1.f / den;
 
-  float acc[16];
+  float4 acc[kNv];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int i = 0; i < kNv; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll(kNv == 4 ? 2 : 4)
   for (int s = 0; s < p.S; ++s) {
     const float w = __shfl_sync(0xffffffffu, w_mine, s);
     if (w == 0.f) continue;  // warp-uniform
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + (((int64_t)t * p.S + s) * p.H + h) * kLatent) +
-                        lane * 4;
+    const float4* src = reinterpret_cast<const float4*>(p.o_part + (((int64_t)t * p.S + s) * p.H + h) * kLatent + d0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kNv; ++i) {
       const float4 v = __ldg(src + i);
-      acc[4 * i + 0] = fmaf(w, v.x, acc[4 * i + 0]);
-      acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
-      acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
-      acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+      acc[i].x = fmaf(w, v.x, acc[i].x);
+      acc[i].y = fmaf(w, v.y, acc[i].y);
+      acc[i].z = fmaf(w, v.z, acc[i].z);
+      acc[i].w = fmaf(w, v.w, acc[i].w);
     }
   }
-  uint32_t packed[8];
+  uint32_t packed[2 * kNv];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    packed[i] = bf16x2_bits(__floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv));
-  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  if (p.lse != nullptr && lane == 0) p.lse[pair] = M + log2f(den) * kLn2;
+  for (int i = 0; i < kNv; ++i) {
+    packed[2 * i] = bf16x2_bits(__floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv));
+    packed[2 * i + 1] = bf16x2_bits(__floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv));
+  }
+  if constexpr (kNv == 1) {
+    *dst = make_uint2(packed[0], packed[1]);
+  } else {  // 16-byte stores
+#pragma unroll
+    for (int i = 0; i < kNv / 2; ++i)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  }
+  if (writes_lse) p.lse[pair] = M + log2f(den) * kLn2;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t pairs = (int64_t)p.T * p.H;
   if (pairs == 0) return cudaSuccess;
+  // Warps per pair: as many as keep the grid within one wave of 32 warps per SM.
+  constexpr int64_t kWaveWarps = 152 * 32;
+  const int wpp = pairs * 4 <= kWaveWarps ? 4 : pairs * 2 <= kWaveWarps ? 2 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((pairs + 7) / 8), 1, 1);
+  cfg.gridDim = dim3((unsigned)((pairs * wpp + 7) / 8), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -86,7 +107,9 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_combine_kernel, p);
+  if (wpp == 4) return cudaLaunchKernelEx(&cfg, lse_combine_kernel<4>, p);
+  if (wpp == 2) return cudaLaunchKernelEx(&cfg, lse_combine_kernel<2>, p);
+  return cudaLaunchKernelEx(&cfg, lse_combine_kernel<1>, p);
 }
 
 }  // namespace smd

@@ -135,6 +135,25 @@ def test_lse_combine_matches_oracle(S, with_sink):
     assert_lse_close(lse, rl, f"combine S={S}")
 
 
+@pytest.mark.parametrize("T,H", [(16, 128), (24, 128), (1, 1216)])
+def test_lse_combine_every_warps_per_pair_choice(T, H):
+    """The combine launch gives each (token, head) 4, 2 or 1 warps by the pair count
+    (here 2048 and 3072 pairs, and 1216, the largest count that takes 4)."""
+    gen = torch.Generator().manual_seed(T * 1000 + H)
+    S = 5
+    o = torch.randn(T, S, H, 512, generator=gen)
+    l = torch.randn(T, S, H, generator=gen) * 3
+    l[0, 1, :] = -math.inf
+    l[T - 1, :, 7] = -math.inf
+    sink = torch.randn(H, generator=gen)
+    out, lse = api.lse_combine(o.cuda(), l.cuda(), sink.cuda())
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_combine(o.double().numpy().transpose(1, 0, 2, 3), l.double().numpy().transpose(1, 0, 2),
+                                sink.double().numpy())
+    assert_out_close(out, ro, f"combine T={T} H={H}")
+    assert_lse_close(lse, rl, f"combine T={T} H={H}")
+
+
 # ----------------------------------------------------------------- full decode
 @pytest.mark.parametrize("wi", range(len(synth.WORKLOADS)))
 def test_decode_workloads_full_size(wi):
