@@ -515,7 +515,7 @@ __device__ __forceinline__ void produce_tma(uint8_t* smem, Misc* m, const AttnPa
           if (i0 + i < NI && pc < kTile * F::NN) {
             const bool valid = valid_row(r);
             uint4 lo, hi;
-            dequant16_perm_nz(valid ? v[i] : make_uint4(0, 0, 0, 0), valid ? code[i] : 0u, lo, hi);
+            dequant16_perm_nz(v[i], code[i], valid, lo, hi);
             *reinterpret_cast<uint4*>(stage + stage_off(r, k * 16)) = lo;
             *reinterpret_cast<uint4*>(stage + stage_off(r, k * 16 + 8)) = hi;
             redo |= (valid && code[i] > 134u) ? (1u << i) : 0u;

@@ -120,11 +120,14 @@ __device__ __forceinline__ void dequant16(const uint4 in, float scale, uint4& lo
 // where the true product leaves bf16's range, like the fp32 route).  NaN bytes
 // (s.1111.111) are zeroed first; products that are not finite are zeroed after.
 
-// Zero the bytes of w that encode e4m3 NaN (low 7 bits all ones).
+// Zero the bytes of w that encode e4m3 NaN (low 7 bits all ones).  Adding one to each
+// byte's low 7 bits sets its bit 7 exactly for those bytes (no carry leaves a byte); a
+// byte permute whose selectors have bit 3 set copies each byte's bit 7 over the byte.
 __device__ __forceinline__ uint32_t zero_fp8_nans(uint32_t w) {
-  const uint32_t t = w & 0x7F7F7F7Fu;
-  const uint32_t hit = (t + 0x01010101u) & 0x80808080u;   // bit 7 set where t == 0x7F
-  return w & ~((hit >> 7) * 0xFFu);
+  const uint32_t hit = (w & 0x7F7F7F7Fu) + 0x01010101u;
+  uint32_t mask;
+  asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(mask) : "r"(hit));
+  return w & ~mask;
 }
 // Two bytes (selected by `sel` for __byte_perm) -> two bf16 carrying value / 2^120.
 __device__ __forceinline__ uint32_t fp8x2_to_bf16x2_bits(uint32_t w, uint32_t sel) {
@@ -191,10 +194,22 @@ __device__ __forceinline__ void dequant16_perm_fast(uint4 in, uint32_t code, uin
   hi = make_uint4(r[4], r[5], r[6], r[7]);
 }
 // The fast path for any bytes: NaN encodings are zeroed first (as the exact path does),
-// so it is exact whenever code <= 134.
-__device__ __forceinline__ void dequant16_perm_nz(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
-  dequant16_perm_fast(make_uint4(zero_fp8_nans(in.x), zero_fp8_nans(in.y), zero_fp8_nans(in.z), zero_fp8_nans(in.w)),
-                      code, lo, hi);
+// so it is exact whenever code <= 134.  A row that is not `valid` gets a zero multiplier
+// instead, so its 16 values come out as +0 or -0.
+__device__ __forceinline__ void dequant16_perm_nz(uint4 in, uint32_t code, bool valid, uint4& lo, uint4& hi) {
+  const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
+  const uint32_t sc = valid ? (sb | (sb << 16)) : 0u;
+  const uint32_t w[4] = {zero_fp8_nans(in.x), zero_fp8_nans(in.y), zero_fp8_nans(in.z), zero_fp8_nans(in.w)};
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a, b;
+    place4(w[i], a, b);
+    r[2 * i] = mul_bf16x2(a, sc);
+    r[2 * i + 1] = mul_bf16x2(b, sc);
+  }
+  lo = make_uint4(r[0], r[1], r[2], r[3]);
+  hi = make_uint4(r[4], r[5], r[6], r[7]);
 }
 // Any input (NaN bytes, large or NaN codes): the exact path, then the same reordering.
 __device__ __forceinline__ void dequant16_perm_exact(uint4 in, uint32_t code, uint4& lo, uint4& hi) {

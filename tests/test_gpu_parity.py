@@ -79,9 +79,11 @@ def _poison(cache: torch.Tensor, P: int, slots, kinds=(0, 1, 2, 3)):
         d = page * P * 584 + off * 576
         sc = page * P * 584 + P * 576 + off * 8
         kind = kinds[i % len(kinds)]
-        if kind == 0:
-            flat[d + 5] = 0x7F
+        if kind == 0:                         # a NaN byte at each position of a 32-bit word
             flat[d + 300] = 0xFF
+            flat[d + 5] = 0x7F
+            flat[d + 66] = 0xFF
+            flat[d + 131] = 0x7F
         elif kind == 1:
             flat[sc + 2] = 255
         elif kind == 2:
