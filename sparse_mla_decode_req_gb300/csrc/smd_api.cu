@@ -28,9 +28,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 constexpr int64_t kMaxEntries = 1 << 20;   // K + W per token
 constexpr int32_t kMaxTokens = 65535;      // grid.y limit of the per-token launches
-// Split-selector cost model, in units of one 64-row tile of one CTA: fixed per-CTA work
-// (TMEM allocation, Q staging, epilogue) and the extra combine launch.
-constexpr int kCtaOverheadTiles = 2;
+// Split-selector cost model, in units of one 64-row tile of one CTA pair (about 3 us on
+// GB300): fixed work per pair (TMEM allocation, Q staging, pipeline fill, epilogue; about
+// 12 us) and the extra combine launch.
+constexpr int kCtaOverheadTiles = 4;
 constexpr int kCombineTiles = 1;
 constexpr int kShortEntries = 1024;
 constexpr int kShortCap = 4;

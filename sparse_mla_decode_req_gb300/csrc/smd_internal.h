@@ -6,7 +6,7 @@
 
 namespace smd {
 
-constexpr int kTileRows = 128;    // gathered rows per attention tile
+constexpr int kTileRows = 64;     // rows per split unit (one attention tile)
 constexpr int kMaxSplits = 32;
 
 struct ConvertParams {

@@ -56,14 +56,19 @@ def test_split_selector_rules(lib):
     # long context, low batch: the selector uses many splits to fill the GPU
     s4 = api.select_num_splits(_dims(), 32, 152)
     assert 8 <= s4 <= 32
+    # the workloads' automatic choices: single request 4 (the short-work cap), batch 32
+    # at 2048 entries 2, batch 4 at 2176 entries 17 (one CTA wave, two tiles per split)
+    assert api.select_num_splits(_dims(T=1, H=64, K=512, W=128), 8, 152) == 4
+    assert api.select_num_splits(_dims(T=32, H=128, K=2048, W=0), 0, 152) == 2
+    assert api.select_num_splits(_dims(T=4, H=128, K=2048, W=128), 32, 152) == 17
     # large batch fills the GPU without splitting
     assert api.select_num_splits(_dims(T=256, H=64, K=512, W=128), 0, 152) == 1
-    # every split keeps at least one 128-row tile
+    # every split keeps at least one 64-row tile
     for T in (1, 2, 3, 5, 16):
         for N in (1, 63, 64, 65, 200, 640, 2176):
             d = _dims(T=T, K=N, W=0)
             s = api.select_num_splits(d, 0, 152)
-            tiles = -(-N // 128)
+            tiles = -(-N // 64)
             tps = -(-tiles // s)
             assert (s - 1) * tps < tiles
     # depends on shapes and SM count only (graph-safe): repeatable
