@@ -696,6 +696,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = p.scale * kLog2e;
     const bool pad_warp = (warp & 3) * 32 >= p.H;  // all 32 heads of this warp are padding
+    // head h's sink logit (natural log), read once here rather than at each item's end
+    const float sink_h = (p.S == 1 && p.sink != nullptr && h < p.H) ? __ldg(p.sink + h) : -INFINITY;
     // Exchange buffers (CTA `rank`'s incoming partials) are recomputed at each use (kernel
     // parameters live in the constant bank), which keeps them out of the register budget.
     auto xbuf = [&](uint32_t rank, int b) {
@@ -897,7 +899,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // splits: write the split's normalised fp32 output and sink-free lse.
       float factor = 0.f, lse_v = -INFINITY;
       if (p.S == 1) {
-        const float sink_nat = (p.sink != nullptr && head_ok) ? __ldg(p.sink + h) : -INFINITY;
+        const float sink_nat = sink_h;
         const float ms = sink_nat * kLog2e;
         const float M = fmaxf(m_ref, ms);
         if (M != -INFINITY) {
@@ -911,43 +913,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         lse_v = (m_ref + log2f(l_tot)) * kLn2;
       }
       const int64_t orow_idx = p.S == 1 ? (int64_t)t * p.H + h : ((int64_t)t * p.S + item.split) * p.H + h;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        if (o_live) {
-          tmem_ld32(tmem + lane_base + kColO + hc * 128 + cc * 32, o);
-          tmem_wait_ld();
-          // NoPE columns hold dims in the (d0, d2, d1, d3) order of the stage
-          if (d0 + cc * 32 < kNope) {
+      // Split partials (fp32) go out through a warp-private 4 KB slice of the P buffers
+      // (no UMMA reads them once O is final): per 32-dim chunk lane r writes its head's
+      // 128 bytes as row r, its 16-byte granules XOR-swizzled by r so that 8 consecutive
+      // rows cover all banks; each warp store then writes four whole 128-byte row segments
+      // instead of 16 bytes in each of 32 rows.
+      if (!pad_warp) {
+        uint8_t* wst = sP + warp * 4096;
+        const int ln = tid & 31;
+        const int head0 = (warp & 3) * 32;
+        const int64_t orow0 = orow_idx - ln;  // output row of lane 0's head
+        // 32 columns of O (this thread's head) from TMEM; NoPE columns hold dims in the
+        // (d0, d2, d1, d3) order of the stage, which is undone here.
+        auto load_o_chunk = [&](uint32_t (&o)[32], int col, bool nope) {
+          if (o_live) {
+            tmem_ld32(tmem + lane_base + kColO + col, o);
+            tmem_wait_ld();
+            if (nope) {
 #pragma unroll
-            for (int g4 = 0; g4 < 8; ++g4) {
-              const uint32_t t1 = o[4 * g4 + 1];
-              o[4 * g4 + 1] = o[4 * g4 + 2];
-              o[4 * g4 + 2] = t1;
+              for (int g4 = 0; g4 < 8; ++g4) {
+                const uint32_t t1 = o[4 * g4 + 1];
+                o[4 * g4 + 1] = o[4 * g4 + 2];
+                o[4 * g4 + 2] = t1;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+        };
+        if (p.S == 1) {
+          // bf16 out: each lane stores its head's 64 bytes per chunk directly (staging
+          // measured no faster for these narrower rows).
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            const int dc = d0 + cc * 32;
+            uint32_t o[32];
+            load_o_chunk(o, hc * 128 + cc * 32, dc < kNope);
+            if (head_ok) {
+              uint4* dstv = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (orow_idx * kLatent + dc) * 2);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  wv[e] = bf16x2_bits(__floats2bfloat162_rn(__uint_as_float(o[8 * i + 2 * e]) * factor,
+                                                            __uint_as_float(o[8 * i + 2 * e + 1]) * factor));
+                dstv[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              }
+            }
+            __syncwarp();
+          }
+        } else {
+          // fp32 partials: a 128-byte staging row holds one 32-dim chunk.
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            const int dc = d0 + cc * 32;  // first output dim of the chunk
+            uint32_t o[32];
+            load_o_chunk(o, hc * 128 + cc * 32, dc < kNope);
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              *reinterpret_cast<float4*>(wst + ln * 128 + ((g ^ (ln & 7)) << 4)) =
+                  make_float4(__uint_as_float(o[4 * g]) * factor, __uint_as_float(o[4 * g + 1]) * factor,
+                              __uint_as_float(o[4 * g + 2]) * factor, __uint_as_float(o[4 * g + 3]) * factor);
+            __syncwarp();
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + (ln >> 3), g = ln & 7;  // row r, granule g (dims 4g..4g+3)
+              v[i] = *reinterpret_cast<const float4*>(wst + r * 128 + ((g ^ (r & 7)) << 4));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + (ln >> 3), g = ln & 7;
+              if (head0 + r < p.H) *reinterpret_cast<float4*>(p.o_part + (orow0 + r) * kLatent + dc + 4 * g) = v[i];
             }
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (!head_ok) continue;
-        if (p.S == 1) {
-          uint4* dstv = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (orow_idx * kLatent + d0 + cc * 32) * 2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              wv[e] = bf16x2_bits(__floats2bfloat162_rn(__uint_as_float(o[8 * i + 2 * e]) * factor,
-                                                        __uint_as_float(o[8 * i + 2 * e + 1]) * factor));
-            dstv[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-          }
-        } else {
-          float4* dstv = reinterpret_cast<float4*>(p.o_part + orow_idx * kLatent + d0 + cc * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dstv[i] = make_float4(__uint_as_float(o[4 * i]) * factor, __uint_as_float(o[4 * i + 1]) * factor,
-                                  __uint_as_float(o[4 * i + 2]) * factor, __uint_as_float(o[4 * i + 3]) * factor);
         }
       }
       if (head_ok && half == 0 && hc == 0) {
