@@ -625,12 +625,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sP = smem + kOffP;
   Misc* m = reinterpret_cast<Misc*>(smem + kOffMisc);
 
-  // Launched as a programmatic dependent of the previous kernel in the stream: only the
-  // launch itself overlaps that kernel; everything here waits for its completion.  (No
-  // early trigger for the next kernel: a split combine launched early would pack its
+  // Launched as a programmatic dependent of the previous kernel in the stream (the index
+  // conversion): the setup below touches nothing that kernel writes, so it overlaps that
+  // kernel's tail, and every thread waits for its completion before its role starts.
+  // (No early trigger for the next kernel: a split combine launched early would pack its
   // blocks onto the few SMs this grid leaves free; launched at this grid's exit it
   // spreads over the whole GPU.)
-  grid_dep_wait();
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const uint32_t half = cluster_rank();   // == blockIdx.x & 1
@@ -642,6 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // shared memory, which follows the 1 KB system reservation).  Both CTAs of the pair
   // see the same alignment, so both leave together before any cluster barrier.
   if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    grid_dep_wait();  // the conversion kernel clears the status word first
     if (tid == 0 && p.status != nullptr) atomicOr(p.status, 2u);
     return;
   }
@@ -683,6 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // the peer's barriers exist before anyone arrives on them remotely
   tc_fence_after();
   const uint32_t tmem = m->tmem_base;
+  grid_dep_wait();
 
   // Register budget: the launch gives 128 per thread (512 x 128 = the whole file); the
   // softmax warpgroups take 176 and the producer warpgroups keep 80 (2 x 128 x (176 + 80)
