@@ -46,7 +46,8 @@
 // is rarely rescaled.
 //
 // The kernel is launched as a programmatic dependent of the previous kernel in the
-// stream and waits for it at entry.  Every wait is bounded; a wait that gives up records
+// stream and waits for it after its own set-up (shared memory and TMEM only), before any
+// global access.  Every wait is bounded; a wait that gives up records
 // bit 0 in the status word and the CTA winds down (draining its UMMAs and gathers,
 // freeing TMEM).
 #include <cuda.h>
@@ -58,7 +59,7 @@ namespace smd {
 namespace {
 
 constexpr int kTile = 64;                   // gathered rows per tile (one raw chunk)
-constexpr int kTilesPerSplitUnit = kTileRows / kTile;  // splits are sized in kTileRows units
+constexpr int kTilesPerSplitUnit = kTileRows / kTile;  // tiles per host split unit (kTileRows rows)
 constexpr int kDHalf = 256;                 // latent dims per CTA
 constexpr int kSoftmaxThreads = 256;        // warps 0-7
 constexpr int kGroupThreads = 128;          // one producer warpgroup
