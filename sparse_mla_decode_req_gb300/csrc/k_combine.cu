@@ -62,14 +62,16 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
   float4 acc[kNv];
 #pragma unroll
   for (int i = 0; i < kNv; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll(kNv == 4 ? 2 : 4)
+  // Loads are unconditional (a batch of them in flight per unrolled group); a split of
+  // weight 0 (lse -inf: no valid entries) contributes an exact 0 whatever its row holds.
+#pragma unroll(kNv == 4 ? 2 : kNv == 2 ? 4 : 8)
   for (int s = 0; s < p.S; ++s) {
     const float w = __shfl_sync(0xffffffffu, w_mine, s);
-    if (w == 0.f) continue;  // warp-uniform
     const float4* src = reinterpret_cast<const float4*>(p.o_part + (((int64_t)t * p.S + s) * p.H + h) * kLatent + d0);
 #pragma unroll
     for (int i = 0; i < kNv; ++i) {
-      const float4 v = __ldg(src + i);
+      float4 v = __ldg(src + i);
+      if (w == 0.f) v = make_float4(0.f, 0.f, 0.f, 0.f);
       acc[i].x = fmaf(w, v.x, acc[i].x);
       acc[i].y = fmaf(w, v.y, acc[i].y);
       acc[i].z = fmaf(w, v.z, acc[i].z);

@@ -137,6 +137,31 @@ def test_lse_combine_matches_oracle(S, with_sink):
     assert_lse_close(lse, rl, f"combine S={S}")
 
 
+@pytest.mark.parametrize("S", [3, 17])
+def test_lse_combine_ignores_rows_of_empty_splits(S):
+    """A split with lse -inf has no entries: whatever its partial row holds (NaN here) adds
+    nothing.  The oracle gets the same inputs with those rows zeroed."""
+    gen = torch.Generator().manual_seed(100 + S)
+    T, H = 2, 128
+    o = torch.randn(T, S, H, 512, generator=gen)
+    l = torch.randn(T, S, H, generator=gen) * 3
+    l[0, 1, :] = -math.inf
+    l[1, S - 1, :] = -math.inf
+    o_clean = o.clone()
+    o[0, 1] = math.nan
+    o[1, S - 1] = math.nan
+    o_clean[0, 1] = 0.0
+    o_clean[1, S - 1] = 0.0
+    sink = torch.randn(H, generator=gen)
+    out, lse = api.lse_combine(o.cuda(), l.cuda(), sink.cuda())
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_combine(o_clean.double().numpy().transpose(1, 0, 2, 3), l.double().numpy().transpose(1, 0, 2),
+                                sink.double().numpy())
+    assert torch.isfinite(out.float()).all()
+    assert_out_close(out, ro, f"combine empty splits S={S}")
+    assert_lse_close(lse, rl, f"combine empty splits S={S}")
+
+
 @pytest.mark.parametrize("T,H", [(16, 128), (24, 128), (1, 1216)])
 def test_lse_combine_every_warps_per_pair_choice(T, H):
     """The combine launch gives each (token, head) 4, 2 or 1 warps by the pair count
@@ -191,6 +216,19 @@ def test_decode_small_shapes(H, N, P):
         out, lse = _run(inp, num_splits=ns)
         assert_out_close(out, ro, f"H{H} N{N} P{P} splits {ns}")
         assert_lse_close(lse, rl, f"H{H} N{N} P{P} splits {ns}")
+
+
+@pytest.mark.parametrize("H", [40, 100, 127])
+def test_decode_partial_head_warps(H):
+    """Head counts that leave a later softmax warp partly filled (its padding heads get no
+    output rows) and, for H <= 96, whole warps of padding; single and split outputs."""
+    w = synth.small_workload(num_tokens=3, num_heads=H, topk=520, swa=120, ctx=1500, n_invalid=11)
+    inp = synth.make_inputs(w, seed=H, device="cuda")
+    ro, rl = oracle_decode(inp)
+    for ns in (1, -3, -8):
+        out, lse = _run(inp, num_splits=ns)
+        assert_out_close(out, ro, f"H{H} splits {ns}")
+        assert_lse_close(lse, rl, f"H{H} splits {ns}")
 
 
 def test_decode_without_sink_and_without_lse():
