@@ -189,9 +189,11 @@ SMD_API int smd_gather_dequant(const smd_dims *dims, const uint8_t *kv_cache, co
 /*
  * Step 5 alone: merges S split partials per (token, head).  o_part f32 [T, S, H, 512]
  * holds each split's output normalised over its own entries, lse_part f32 [T, S, H]
- * its natural-log denominator without sink (-inf for an empty split).  Writes
- * out bf16 [T, H, 512] and, if non-NULL, lse f32 [T, H]; sink may be NULL.
- * Requires 1 <= S <= 32 and 1 <= H.
+ * its natural-log denominator without sink (-inf for an empty split; such a split adds
+ * nothing, whatever its o_part row holds).  Writes out bf16 [T, H, 512] and, if
+ * non-NULL, lse f32 [T, H]; sink may be NULL.  With no finite lse and no sink the output
+ * row is 0 and lse is -inf.  Requires 1 <= S <= 32 and 1 <= H; o_part and out 16-byte
+ * aligned.
  */
 SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_heads,
                             const float *o_part, const float *lse_part, const float *sink,
