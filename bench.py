@@ -340,8 +340,8 @@ def main(argv=None):
     roof["launch_ms_mean"] = statistics.mean(attn_ms)
 
     # end to end through the public call with host buffers: h2d of the step's inputs,
-    # decode, d2h of out + lse, per step
-    e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step)
+    # decode, d2h of out + lse, per step (out still holds the device path's result)
+    e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step, device_out=out)
     e2e["seconds"] = max_over_ranks(pg, e2e["seconds"], dev)
     e2e_val = job_rate(rows_per_step, e2e["steps"], world, e2e["seconds"])
 
@@ -365,7 +365,8 @@ def main(argv=None):
         "hbm_gbs_step": 584.0 * rows_per_step / (ms_per_step / 1e3) / 1e9,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "steps": e2e["steps"]},
+                "steps": e2e["steps"], "transfers": "one h2d of the packed inputs, one d2h of out + lse",
+                "matches_device_path": e2e.get("matches_device_path")},
         "gpu_launches": K * (2 + (1 if S > 1 else 0)),
         "clocks": clocks,
         "wall_s_timed_region": wall,
@@ -407,30 +408,54 @@ def load_traffic(name: str):
     return None
 
 
-def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step):
+def pack_layout(named):
+    """Byte layout of (name, tensor) pairs packed back to back at 256-byte offsets:
+    ({name: (offset, nbytes, dtype, shape)}, total bytes)."""
+    lay, off = {}, 0
+    for k, t in named:
+        n = t.numel() * t.element_size()
+        lay[k] = (off, n, t.dtype, tuple(t.shape))
+        off = (off + n + 255) // 256 * 256
+    return lay, max(off, 256)
+
+
+def pack_views(buf, lay):
+    """Typed, shaped views into a flat uint8 buffer laid out by pack_layout."""
+    return {k: buf[o:o + n].view(dt).view(shape) for k, (o, n, dt, shape) in lay.items()}
+
+
+def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step, device_out=None):
+    """The step through the public call with host-resident inputs: every step copies the
+    inputs (packed in one pinned buffer) to the device in one transfer, runs
+    sparse_mla_decode on views of that buffer, and reads out and lse (one device buffer)
+    back in one transfer."""
     import torch
-    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("q", "block_table", "req_id", "topk_idx", "swa_idx")}
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    names = [k for k in ("q", "block_table", "req_id", "topk_idx", "swa_idx")
+             if not (k == "topk_idx" and not w.topk) and not (k == "swa_idx" and not w.swa)]
+    src = {k: getattr(inp, k).cpu() for k in names}
+    lay_in, nb_in = pack_layout([(k, src[k]) for k in names])
+    h_in = torch.zeros(nb_in, dtype=torch.uint8).pin_memory()
+    for k, v in pack_views(h_in, lay_in).items():
+        v.copy_(src[k])
+    d_in = torch.empty(nb_in, dtype=torch.uint8, device=dev)
+    dbuf = pack_views(d_in, lay_in)
     T, H = w.num_tokens, w.num_heads
-    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
-    h_out = torch.empty(T, H, 512, dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    lay_out, nb_out = pack_layout([("out", torch.empty(T, H, 512, dtype=torch.bfloat16)),
+                                   ("lse", torch.empty(T, H, dtype=torch.float32))])
+    d_res = torch.empty(nb_out, dtype=torch.uint8, device=dev)
+    res = pack_views(d_res, lay_out)
+    h_res = torch.empty(nb_out, dtype=torch.uint8).pin_memory()
     dims = api.make_dims(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
-                         dbuf["topk_idx"] if w.topk else None, dbuf["swa_idx"] if w.swa else None, w.block_size)
+                         dbuf.get("topk_idx"), dbuf.get("swa_idx"), w.block_size)
     ws = torch.empty(api.workspace_size(dims, w.max_splits, 0), dtype=torch.uint8, device=dev)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
 
     def one():
-        for k, v in host.items():
-            dbuf[k].copy_(v, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         api.sparse_mla_decode(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
-                              dbuf["topk_idx"] if w.topk else None, dbuf["swa_idx"] if w.swa else None,
-                              inp.sink, inp.scale, out=out, lse=lse, num_splits=w.max_splits, workspace=ws,
+                              dbuf.get("topk_idx"), dbuf.get("swa_idx"), inp.sink, inp.scale,
+                              out=res["out"], lse=res["lse"], num_splits=w.max_splits, workspace=ws,
                               block_size=w.block_size)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(3):
         one()
@@ -443,7 +468,10 @@ def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step):
         b.record(stream)
     torch.cuda.synchronize()
     secs = sum(a.elapsed_time(b) for a, b in evs) / 1e3
-    return {"seconds": secs, "steps": steps, "h2d": h2d, "d2h": d2h}
+    r = {"seconds": secs, "steps": steps, "h2d": nb_in, "d2h": nb_out}
+    if device_out is not None:  # same inputs, same kernels: the results must agree bit for bit
+        r["matches_device_path"] = bool(torch.equal(pack_views(h_res, lay_out)["out"], device_out.cpu()))
+    return r
 
 
 if __name__ == "__main__":

@@ -34,7 +34,7 @@ def _worker(rank: int, world: int, port: int, out):
 
 def test_two_cpu_ranks_share_the_slowest_time():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
     assert sorted(out.keys()) == [0, 1]
     for rank in range(world):
