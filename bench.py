@@ -341,9 +341,14 @@ def main(argv=None):
 
     # end to end through the public call with host buffers: h2d of the step's inputs,
     # decode, d2h of out + lse, per step (out still holds the device path's result)
-    e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step, device_out=out)
-    e2e["seconds"] = max_over_ranks(pg, e2e["seconds"], dev)
-    e2e_val = job_rate(rows_per_step, e2e["steps"], world, e2e["seconds"])
+    try:
+        e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step, device_out=out)
+    except Exception as exc:  # keep the device-timed line; the failure is reported in it
+        e2e = {"seconds": None, "steps": 0, "h2d": 0, "d2h": 0, "error": repr(exc)[:300]}
+        print(f"e2e leg failed: {exc!r}", file=sys.stderr)
+    # every rank joins the reduction (a failed leg contributes +inf, which voids the value)
+    secs = max_over_ranks(pg, e2e["seconds"] if e2e["seconds"] is not None else float("inf"), dev)
+    e2e_val = job_rate(rows_per_step, e2e["steps"], world, secs) if secs != float("inf") else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -366,7 +371,7 @@ def main(argv=None):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e["steps"], "transfers": "one h2d of the packed inputs, one d2h of out + lse",
-                "matches_device_path": e2e.get("matches_device_path")},
+                "matches_device_path": e2e.get("matches_device_path"), **({"error": e2e["error"]} if "error" in e2e else {})},
         "gpu_launches": K * (2 + (1 if S > 1 else 0)),
         "clocks": clocks,
         "wall_s_timed_region": wall,
