@@ -116,22 +116,22 @@ def _stream(stream):
 def _row_stride(t, n_cols):
     if t is None or n_cols == 0:
         return max(n_cols, 0)
-    assert t.dtype == torch.int32 and t.dim() == 2 and t.stride(1) == 1, \
+    st = t.stride()
+    assert t.dtype is torch.int32 and len(st) == 2 and st[1] == 1, \
         "index tensors: int32 [rows, cols], unit column stride"
-    return t.stride(0)
+    return st[0]
 
 
 def make_dims(q, kv_cache, block_table, req_id, topk_idx, swa_idx, block_size: int = 64) -> Dims:
     """smd_dims from tensor shapes (q [T,H,512], kv_cache [pages, P*584], block_table [R, B])."""
-    T = int(req_id.shape[0])
-    H = int(q.shape[1]) if q is not None else 1
-    K = 0 if topk_idx is None else int(topk_idx.shape[1])
-    W = 0 if swa_idx is None else int(swa_idx.shape[1])
-    return Dims(num_tokens=T, num_heads=H, num_requests=int(block_table.shape[0]),
-                max_blocks_per_req=int(block_table.shape[1]), num_pages=int(kv_cache.shape[0]),
-                block_size=int(block_size), topk=K, swa=W, pad_=0,
-                bt_stride=_row_stride(block_table, int(block_table.shape[1])),
-                topk_stride=_row_stride(topk_idx, K), swa_stride=_row_stride(swa_idx, W))
+    T = req_id.shape[0]
+    H = q.shape[1] if q is not None else 1
+    K = 0 if topk_idx is None else topk_idx.shape[1]
+    W = 0 if swa_idx is None else swa_idx.shape[1]
+    R, B = block_table.shape
+    # positional, in smd_dims field order (cheaper than keywords on every call)
+    return Dims(T, H, R, B, kv_cache.shape[0], int(block_size), K, W, 0,
+                _row_stride(block_table, B), _row_stride(topk_idx, K), _row_stride(swa_idx, W))
 
 
 def select_num_splits(dims: Dims, num_splits: int = 0, num_sms: int = 0) -> int:
