@@ -97,10 +97,12 @@ typedef struct smd_dims {
  * split-K parts S the decode will use, or a negative status.  num_splits: 0 = automatic
  * with cap 32; n > 0 = automatic with cap n; n < 0 = exactly -n (1..32).  The automatic
  * choice depends only on the shapes and num_sms, so a captured CUDA graph stays valid:
- * "short" steps (K+W <= 1024 entries) cap at 4 splits; otherwise the count that
- * minimises (CTA waves x tiles per split) over 1..cap, each split keeping >= 1 tile
- * (vLLM PR #52212 report, "实现拆解" item 2: occupancy target, short work <= 4, low-batch
- * long context up to 32).  num_sms <= 0 means "the current device's SM count".
+ * the S in 1..cap (cap at most 4 for "short" steps, K+W <= 1024 entries) that minimises
+ * waves x (tiles per split + 4) + (S > 1 ? 1 : 0), with 64-row tiles, waves =
+ * ceil(T x S x 2 / num_sms) (one CTA pair per token and split) and 4 and 1 the fixed cost
+ * of a pair and of the combine in tiles; every split keeps >= 1 tile (vLLM PR #52212
+ * report, "实现拆解" item 2: occupancy target, short work <= 4, low-batch long context up
+ * to 32).  num_sms <= 0 means "the current device's SM count".
  */
 SMD_API int smd_select_num_splits(const smd_dims *dims, int num_splits, int num_sms);
 
