@@ -125,5 +125,41 @@ def test_null_pointers_rejected(lib):
     assert lib.smd_read_status(None, ctypes.byref(v), None) == api.SMD_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("T,S,H", [(2, 0, 4), (2, 33, 4), (2, 3, 0), (-1, 3, 4)])
+def test_combine_bad_shapes_rejected(lib, T, S, H):
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    rc = lib.smd_lse_combine(T, S, H, p, p, None, p, None, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "combine shape" in api.last_error()
+
+
+def test_combine_alignment_and_empty_batch(lib):
+    buf = ctypes.create_string_buffer(8192)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    al, mis = ctypes.c_void_p(base), ctypes.c_void_p(base + 4)
+    for o_part, out in ((mis, al), (al, mis)):
+        rc = lib.smd_lse_combine(2, 3, 4, o_part, al, None, out, None, None)
+        assert rc == api.SMD_ERR_INVALID_ARG and "aligned" in api.last_error()
+    # no tokens: nothing to do, and no pointer is looked at
+    assert lib.smd_lse_combine(0, 3, 4, None, None, None, None, None, None) == api.SMD_OK
+
+
+def test_gather_and_attention_host_checks(lib):
+    d = _dims(T=2)
+    buf = ctypes.create_string_buffer(8192)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    al, mis = ctypes.c_void_p(base), ctypes.c_void_p(base + 8)
+    rc = lib.smd_gather_dequant(ctypes.byref(d), mis, al, 5, al, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "aligned" in api.last_error()
+    assert lib.smd_gather_dequant(ctypes.byref(d), None, None, 0, None, None) == api.SMD_OK
+    ad = api.attention_dims(2, 64, 640, 100)
+    rc = lib.smd_sparse_mla_attention(ctypes.byref(ad), al, al, al, None, ctypes.c_float(1.0), -33, al, None,
+                                      None, None, None, al, ctypes.c_size_t(1 << 20), None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "num_splits" in api.last_error()
+    ad0 = api.attention_dims(0, 64, 640, 100)
+    assert lib.smd_sparse_mla_attention(ctypes.byref(ad0), None, None, None, None, ctypes.c_float(1.0), 0, None,
+                                        None, None, None, None, None, ctypes.c_size_t(0), None) == api.SMD_OK
+
+
 def test_version(lib):
     assert lib.smd_version() >= 100
