@@ -269,10 +269,9 @@ def main(argv=None):
     P = api._ptr
     conv_args = (ctypes.byref(dims), P(inp.block_table), P(inp.req_id), P(topk), P(swa), P(gidx), sp)
     attn_dims = api.attention_dims(T, H, N, inp.num_pages, w.block_size)
-    xchg = torch.empty(api.attention_xchg_size(attn_dims, w.max_splits, sms), dtype=torch.uint8, device=dev)
     attn_args = (ctypes.byref(attn_dims), P(inp.q), P(inp.kv_cache), P(gidx), P(inp.sink),
                  ctypes.c_float(inp.scale), int(w.max_splits), P(out), P(lse), P(o_part), P(lse_part),
-                 P(status), P(xchg), ctypes.c_size_t(xchg.numel()), sp)
+                 P(status), sp)
     comb_args = (T, S, H, P(o_part), P(lse_part), P(inp.sink), P(out), P(lse), sp)
 
     def step():

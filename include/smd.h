@@ -68,7 +68,8 @@ enum {
   SMD_ERR_UNSUPPORTED = -2,
   SMD_ERR_WORKSPACE = -3,
   SMD_ERR_CUDA = -4,
-  SMD_ERR_TIMEOUT = -5
+  SMD_ERR_TIMEOUT = -5,
+  SMD_ERR_DEVICE_CHECK = -6
 };
 
 #define SMD_LATENT_DIM 512
@@ -98,31 +99,23 @@ typedef struct smd_dims {
  * with cap 32; n > 0 = automatic with cap n; n < 0 = exactly -n (1..32).  The automatic
  * choice depends only on the shapes and num_sms, so a captured CUDA graph stays valid:
  * the S in 1..cap (cap at most 4 for "short" steps, K+W <= 1024 entries) that minimises
- * waves x (tiles per split + 4) + (S > 1 ? 1 : 0), with 64-row tiles, waves =
- * ceil(T x S x 2 / num_sms) (one CTA pair per token and split) and 4 and 1 the fixed cost
- * of a pair and of the combine in tiles; every split keeps >= 1 tile (vLLM PR #52212
- * report, "实现拆解" item 2: occupancy target, short work <= 4, low-batch long context up
- * to 32).  num_sms <= 0 means "the current device's SM count".
+ * waves x (tiles per split + 4) + (S > 1 ? 2 : 0), with 64-row tiles, waves =
+ * ceil(T x S x ceil(H / 64) / num_sms) (one CTA per token, split and group of 64 heads,
+ * one CTA per SM) and 4 and 2 the fixed cost of a work item and of the combine in tiles;
+ * every split keeps >= 1 tile (vLLM PR #52212 report, "实现拆解" item 2: occupancy
+ * target, short work <= 4, low-batch long context up to 32).  num_sms <= 0 means "the
+ * current device's SM count".
  */
 SMD_API int smd_select_num_splits(const smd_dims *dims, int num_splits, int num_sms);
 
 /*
  * Device workspace bytes smd_sparse_mla_decode needs for the given split request
- * (same num_splits/num_sms meaning as smd_select_num_splits).  Holds a status word,
- * the converted indices [T, K+W] int32, when S > 1 the split partials o_part f32
- * [T, S, H, 512] and lse_part f32 [T, S, H], and the attention kernel's exchange
- * buffers (smd_attention_xchg_size).  Returns 0 on bad dims.
+ * (same num_splits/num_sms meaning as smd_select_num_splits): a 256-byte status word,
+ * the converted indices [T, K+W] int32 and, when S > 1, the split partials o_part f32
+ * [T, S, H, 512] and lse_part f32 [T, S, H], each 256-byte aligned.  Returns 0 on bad
+ * dims.
  */
 SMD_API size_t smd_workspace_size(const smd_dims *dims, int num_splits, int num_sms);
-
-/*
- * Device bytes of the exchange buffers smd_sparse_mla_attention needs: the two CTAs that
- * share a (token, split) work item each hold half of the 512 latent dims, and swap their
- * fp32 partial QK scores of every 64-entry tile through these buffers (two 32 KB buffers
- * per CTA, one CTA pair per two SMs, at most min(T * S, num_sms / 2) pairs).  The content
- * is scratch: nothing is read before the same call writes it.  Returns 0 on bad dims.
- */
-SMD_API size_t smd_attention_xchg_size(const smd_dims *dims, int num_splits, int num_sms);
 
 /*
  * The whole decode step (conversion, fused gather + dequant + tcgen05 attention, and
@@ -158,16 +151,13 @@ SMD_API int smd_sparse_mla_decode(const smd_dims *dims, const void *q, const uin
  * S > 1: writes each split's normalised output o_part f32 [T, S, H, 512] and its
  * sink-free lse_part f32 [T, S, H] (-inf for a split without valid entries), to be
  * merged by smd_lse_combine; out/lse are not touched.  status (optional, device int32)
- * gets bit 0 set if a bounded wait inside the kernel gives up (bit 1 if the kernel's
- * shared memory was not 1024-byte aligned; nothing is computed then).  xchg: device
- * scratch of xchg_bytes >= smd_attention_xchg_size(dims, num_splits, device SMs),
- * 16-byte aligned (SMD_ERR_WORKSPACE if smaller).  dims->topk + dims->swa is the row
- * length of gidx; the index pointers of dims are not used.
+ * gets bit 0 set if a bounded wait inside the kernel gives up.  dims->topk + dims->swa
+ * is the row length of gidx; the index pointers of dims are not used.
  */
 SMD_API int smd_sparse_mla_attention(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
                                      const int32_t *gidx, const float *sink, float scale, int num_splits,
                                      void *out, float *lse, float *o_part, float *lse_part,
-                                     int32_t *status, void *xchg, size_t xchg_bytes, smd_stream_t stream);
+                                     int32_t *status, smd_stream_t stream);
 
 /*
  * Step 1 alone: writes gidx i32 [T, K+W] (top-k entries first, window entries at
@@ -233,6 +223,18 @@ SMD_API int smd_sparse_mla_decode_static_scratch(const smd_dims *dims, const voi
                                                  const int32_t *topk_idx, const int32_t *swa_idx,
                                                  const float *sink, float scale, void *out, float *lse,
                                                  int num_splits, smd_stream_t stream);
+
+/*
+ * Test and fault-injection hook (not part of the decode semantics): sets the bound, in
+ * nanoseconds of wall time, of every pipeline wait inside the attention kernel for launches
+ * made after the call, process-wide; 0 restores the default of 2 s.  Returns the previous
+ * bound.  A bound far below a tile's run time makes the waits give up on purpose: the
+ * kernel then records bit 0 in its status word, drains the work it has in flight (those
+ * waits keep a 2 s bound), frees its tensor memory and returns, so the context stays
+ * usable and smd_read_status reports SMD_ERR_TIMEOUT.  Outputs of such a launch are
+ * undefined.
+ */
+SMD_API uint64_t smd_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 SMD_API const char *smd_last_error(void);

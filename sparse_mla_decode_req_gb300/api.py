@@ -21,6 +21,7 @@ SMD_ERR_UNSUPPORTED = -2
 SMD_ERR_WORKSPACE = -3
 SMD_ERR_CUDA = -4
 SMD_ERR_TIMEOUT = -5
+SMD_ERR_DEVICE_CHECK = -6
 LATENT_DIM = 512
 ROW_BYTES = 584
 MAX_SPLITS = 32
@@ -60,9 +61,9 @@ _SIGS = {
     "smd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int]),
     "smd_sparse_mla_decode": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
                                              _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
-    "smd_attention_xchg_size": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int]),
     "smd_sparse_mla_attention": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, ctypes.c_float, ctypes.c_int,
-                                                _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+                                                _P, _P, _P, _P, _P, _P]),
+    "smd_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "smd_convert_req_index": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, _P, _P, _P, _P]),
     "smd_gather_dequant": (ctypes.c_int, [ctypes.POINTER(Dims), _P, _P, ctypes.c_int64, _P, _P]),
     "smd_lse_combine": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P]),
@@ -168,13 +169,6 @@ def sparse_mla_decode(q, kv_cache, block_table, req_id, topk_idx, swa_idx, sink,
     return out, lse
 
 
-def attention_xchg_size(dims: Dims, num_splits: int = 0, num_sms: int = 0) -> int:
-    n = load().smd_attention_xchg_size(ctypes.byref(dims), int(num_splits), int(num_sms))
-    if n == 0:
-        raise SmdError(SMD_ERR_INVALID_ARG, last_error())
-    return int(n)
-
-
 def attention_dims(T: int, H: int, N: int, num_pages: int, block_size: int = 64) -> Dims:
     """smd_dims for the attention-only call over converted slots [T, N]."""
     return Dims(num_tokens=T, num_heads=H, num_requests=1, max_blocks_per_req=1, num_pages=int(num_pages),
@@ -183,12 +177,11 @@ def attention_dims(T: int, H: int, N: int, num_pages: int, block_size: int = 64)
 
 def sparse_mla_attention(q, kv_cache, gidx, sink, scale: float, num_pages: int | None = None, num_splits: int = 0,
                          out=None, lse=None, o_part=None, lse_part=None, status=None, block_size: int = 64,
-                         stream=None, xchg=None):
+                         stream=None):
     """Fused gather + dequant + attention over converted slots gidx int32 [T, N].
 
     One split: returns (out, lse).  Several splits: returns (o_part, lse_part), the
-    per-split partials for ``lse_combine``.  ``xchg`` is the kernel's exchange scratch
-    (allocated here when not given).
+    per-split partials for ``lse_combine``.
     """
     T, N = int(gidx.shape[0]), int(gidx.shape[1])
     H = int(q.shape[1])
@@ -196,8 +189,6 @@ def sparse_mla_attention(q, kv_cache, gidx, sink, scale: float, num_pages: int |
     sms = torch.cuda.get_device_properties(q.device).multi_processor_count
     S = select_num_splits(dims, num_splits, sms)
     dev = q.device
-    if xchg is None:
-        xchg = torch.empty(attention_xchg_size(dims, num_splits, sms), dtype=torch.uint8, device=dev)
     if S == 1 and out is None:
         out = torch.empty(T, H, LATENT_DIM, dtype=torch.bfloat16, device=dev)
     if S == 1 and lse is None:
@@ -209,8 +200,7 @@ def sparse_mla_attention(q, kv_cache, gidx, sink, scale: float, num_pages: int |
     assert gidx.dtype == torch.int32 and gidx.is_contiguous()
     _check(load().smd_sparse_mla_attention(ctypes.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(gidx), _ptr(sink),
                                            ctypes.c_float(scale), int(num_splits), _ptr(out), _ptr(lse),
-                                           _ptr(o_part), _ptr(lse_part), _ptr(status), _ptr(xchg),
-                                           ctypes.c_size_t(xchg.numel() * xchg.element_size()), _stream(stream)))
+                                           _ptr(o_part), _ptr(lse_part), _ptr(status), _stream(stream)))
     return (out, lse) if S == 1 else (o_part, lse_part)
 
 
@@ -264,3 +254,9 @@ def read_status(workspace, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check(load().smd_read_status(_ptr(workspace), ctypes.byref(v), _stream(stream)))
     return v.value
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    """Bound of the attention kernel's pipeline waits for later launches (0 = default 2 s);
+    returns the previous bound.  A test hook: a tiny bound makes the waits give up."""
+    return int(load().smd_set_wait_limit_ns(ctypes.c_uint64(int(limit_ns))))

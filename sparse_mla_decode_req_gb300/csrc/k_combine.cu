@@ -98,7 +98,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t pairs = (int64_t)p.T * p.H;
   if (pairs == 0) return cudaSuccess;
   // Warps per pair: as many as keep the grid within one wave of 32 warps per SM.
-  constexpr int64_t kWaveWarps = 152 * 32;
+  const int64_t kWaveWarps = (int64_t)(p.sms > 0 ? p.sms : 1) * 32;
   const int wpp = pairs * 4 <= kWaveWarps ? 4 : pairs * 2 <= kWaveWarps ? 2 : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((pairs * wpp + 7) / 8), 1, 1);

@@ -7,7 +7,9 @@
 //
 // One warp per row.  Lane L writes output dims [16L, 16L+16): lanes 0..27 read 16 NoPE
 // bytes and one scale code, lanes 28..31 read 32 RoPE bytes; every load and store is
-// 16 bytes wide and a warp's output row is one contiguous 1 KB write.
+// 16 bytes wide and a warp's output row is one contiguous 1 KB write.  The NoPE pieces go
+// through dequant_piece and the RoPE pieces through scrub_bf16x8, the same routines the
+// attention kernel's converters run, so this export pins the hot path's dequantisation.
 #include "smd_device.cuh"
 #include "smd_internal.h"
 
@@ -25,7 +27,7 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherParams p) {
     const uint8_t* data = row_data(c, slot);
     if (lane < 28) {
       const uint4 raw = ldg16<ALIGN16>(data + lane * 16);
-      dequant16_fast(raw, __ldg(row_scales(c, slot) + (lane >> 2)), lo, hi);
+      dequant_piece(raw, __ldg(row_scales(c, slot) + (lane >> 2)), lo, hi);
     } else {
       lo = scrub_bf16x8(ldg16<ALIGN16>(data + kNope + (lane - 28) * 32));
       hi = scrub_bf16x8(ldg16<ALIGN16>(data + kNope + (lane - 28) * 32 + 16));

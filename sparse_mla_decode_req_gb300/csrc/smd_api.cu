@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "smd.h"
 #include "smd_internal.h"
 
@@ -28,11 +30,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 constexpr int64_t kMaxEntries = 1 << 20;   // K + W per token
 constexpr int32_t kMaxTokens = 65535;      // grid.y limit of the per-token launches
-// Split-selector cost model, in units of one 64-row tile of one CTA pair (about 3 us on
-// GB300): fixed work per pair (TMEM allocation, Q staging, pipeline fill, epilogue; about
-// 12 us) and the extra combine launch.
+// Split-selector cost model, in units of one 64-row tile of one CTA: fixed work per work
+// item (Q load, pipeline fill, epilogue) and the extra combine launch.
 constexpr int kCtaOverheadTiles = 4;
-constexpr int kCombineTiles = 1;
+constexpr int kCombineTiles = 2;
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 constexpr int kShortEntries = 1024;
 constexpr int kShortCap = 4;
 
@@ -81,13 +84,13 @@ int select_splits(const smd_dims* d, int request, int sms) {
   if (N <= kShortEntries && cap > kShortCap) cap = kShortCap;
   if (tiles < cap) cap = (int)(tiles > 0 ? tiles : 1);
   if (d->num_tokens == 0 || tiles == 0) return 1;
-  const int64_t cps = smd::attn_ctas_per_split();
+  const int64_t cps = smd::attn_ctas_per_split(d->num_heads);
   int best = 1;
   int64_t best_cost = INT64_MAX;
   for (int s = 1; s <= cap; ++s) {
     const int64_t tps = (tiles + s - 1) / s;
     if ((int64_t)(s - 1) * tps >= tiles) continue;  // would leave a split without a tile
-    const int64_t ctas = (int64_t)d->num_tokens * s * cps;
+    const int64_t ctas = (int64_t)d->num_tokens * s * cps;  // one CTA per SM
     const int64_t waves = (ctas + sms - 1) / sms;
     const int64_t cost = waves * (tps + kCtaOverheadTiles) + (s > 1 ? kCombineTiles : 0);
     if (cost < best_cost) {
@@ -99,17 +102,12 @@ int select_splits(const smd_dims* d, int request, int sms) {
 }
 
 struct Layout {
-  size_t status = 0, gidx = 0, o_part = 0, lse_part = 0, xchg = 0, total = 0;
+  size_t status = 0, gidx = 0, o_part = 0, lse_part = 0, total = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Exchange-buffer bytes of the attention launch for T tokens in S splits on `sms` SMs.
-size_t xchg_need(const smd_dims* d, int S, int sms) {
-  return smd::attn_xchg_bytes(smd::attn_pairs((int64_t)d->num_tokens * S, sms));
-}
-
-Layout workspace_layout(const smd_dims* d, int S, int sms) {
+Layout workspace_layout(const smd_dims* d, int S) {
   Layout L;
   const size_t T = (size_t)d->num_tokens, N = (size_t)d->topk + (size_t)d->swa, H = (size_t)d->num_heads;
   size_t off = 0;
@@ -123,10 +121,39 @@ Layout workspace_layout(const smd_dims* d, int S, int sms) {
     L.lse_part = off;
     off += up256(T * (size_t)S * H * sizeof(float));
   }
-  L.xchg = off;
-  off += up256(xchg_need(d, S, sms));
   L.total = off;
   return L;
+}
+
+// Attention launch parameters shared by the whole-step and the stage entry points.
+smd::AttnParams attn_params(const smd_dims* d, int S, int sms, const void* q, const uint8_t* cache,
+                            const int32_t* gidx, const float* sink, float scale, void* out, float* lse,
+                            float* o_part, float* lse_part, uint32_t* status) {
+  const int64_t N = (int64_t)d->topk + d->swa;
+  const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
+  smd::AttnParams a{};
+  a.q = q;
+  a.cache = cache;
+  a.gidx = gidx;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.o_part = S > 1 ? o_part : nullptr;
+  a.lse_part = S > 1 ? lse_part : nullptr;
+  a.status = status;
+  a.scale = scale;
+  a.num_pages = d->num_pages;
+  a.T = d->num_tokens;
+  a.H = d->num_heads;
+  a.N = (int32_t)N;
+  a.P = d->block_size;
+  a.S = S;
+  a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
+  if (a.tiles_per_split < 1) a.tiles_per_split = 1;
+  a.HG = smd::attn_ctas_per_split(d->num_heads);
+  a.G = smd::attn_ctas((int64_t)a.T * S * a.HG, sms);
+  a.wait_limit_ns = smd::wait_limit_ns();
+  return a;
 }
 
 smd::ConvertParams convert_params(const smd_dims* d, const int32_t* bt, const int32_t* req,
@@ -163,6 +190,8 @@ int check_index_ptrs(const smd_dims* d, const int32_t* bt, const int32_t* req, c
 }  // namespace
 
 namespace smd {
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 int set_error(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -191,13 +220,11 @@ SMD_API int smd_select_num_splits(const smd_dims* dims, int num_splits, int num_
 SMD_API size_t smd_workspace_size(const smd_dims* dims, int num_splits, int num_sms) {
   const int S = smd_select_num_splits(dims, num_splits, num_sms);
   if (S < 1) return 0;
-  return workspace_layout(dims, S, device_sms(num_sms)).total;
+  return workspace_layout(dims, S).total;
 }
 
-SMD_API size_t smd_attention_xchg_size(const smd_dims* dims, int num_splits, int num_sms) {
-  const int S = smd_select_num_splits(dims, num_splits, num_sms);
-  if (S < 1) return 0;
-  return xchg_need(dims, S, device_sms(num_sms));
+SMD_API uint64_t smd_set_wait_limit_ns(uint64_t limit_ns) {
+  return g_wait_limit_ns.exchange(limit_ns == 0 ? kDefaultWaitLimitNs : limit_ns);
 }
 
 SMD_API int smd_convert_req_index(const smd_dims* dims, const int32_t* block_table, const int32_t* req_id,
@@ -239,7 +266,9 @@ SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_
   if (num_tokens == 0) return SMD_OK;
   if (o_part == nullptr || lse_part == nullptr || out == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned16(o_part) || !aligned16(out)) return fail(SMD_ERR_INVALID_ARG, "o_part/out not 16-byte aligned");
-  smd::CombineParams p{o_part, lse_part, sink, out, lse, num_tokens, num_splits, num_heads};
+  const int sms = device_sms(0);
+  if (sms <= 0) return fail(SMD_ERR_CUDA, "cannot query the device SM count");
+  smd::CombineParams p{o_part, lse_part, sink, out, lse, num_tokens, num_splits, num_heads, sms};
   const cudaError_t e = smd::launch_combine(p, stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "combine launch");
 }
@@ -265,7 +294,7 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   const int sms = device_sms(0);
   if (sms <= 0) return fail(SMD_ERR_CUDA, "cannot query the device SM count");
   const int S = select_splits(dims, num_splits, sms);
-  const Layout L = workspace_layout(dims, S, sms);
+  const Layout L = workspace_layout(dims, S);
   if (workspace_bytes < L.total)
     return fail(SMD_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -277,33 +306,13 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   if (dims->num_tokens == 0) return SMD_OK;
 
-  const int64_t N = (int64_t)dims->topk + dims->swa;
-  const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
-  smd::AttnParams a{};
-  a.q = q;
-  a.cache = kv_cache;
-  a.gidx = gidx;
-  a.sink = sink;
-  a.out = out;
-  a.lse = lse;
-  a.o_part = S > 1 ? reinterpret_cast<float*>(ws + L.o_part) : nullptr;
-  a.lse_part = S > 1 ? reinterpret_cast<float*>(ws + L.lse_part) : nullptr;
-  a.status = status;
-  a.xchg = ws + L.xchg;
-  a.scale = scale;
-  a.num_pages = dims->num_pages;
-  a.T = dims->num_tokens;
-  a.H = dims->num_heads;
-  a.N = (int32_t)N;
-  a.P = dims->block_size;
-  a.S = S;
-  a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
-  if (a.tiles_per_split < 1) a.tiles_per_split = 1;
-  a.G = smd::attn_pairs((int64_t)a.T * S, sms);
+  const smd::AttnParams a =
+      attn_params(dims, S, sms, q, kv_cache, gidx, sink, scale, out, lse, reinterpret_cast<float*>(ws + L.o_part),
+                  reinterpret_cast<float*>(ws + L.lse_part), status);
   e = smd::launch_attn(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (S > 1) {
-    smd::CombineParams c{a.o_part, a.lse_part, sink, out, lse, dims->num_tokens, S, dims->num_heads};
+    smd::CombineParams c{a.o_part, a.lse_part, sink, out, lse, dims->num_tokens, S, dims->num_heads, sms};
     e = smd::launch_combine(c, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
@@ -313,7 +322,7 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
 SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
                                      const int32_t* gidx, const float* sink, float scale, int num_splits,
                                      void* out, float* lse, float* o_part, float* lse_part, int32_t* status,
-                                     void* xchg, size_t xchg_bytes, smd_stream_t stream) {
+                                     smd_stream_t stream) {
   g_err[0] = '\0';
   const int rc = check_dims(dims);
   if (rc != SMD_OK) return rc;
@@ -331,31 +340,8 @@ SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const 
   if (!aligned16(q) || !aligned16(kv_cache) || (out != nullptr && !aligned16(out)) ||
       (o_part != nullptr && !aligned16(o_part)))
     return fail(SMD_ERR_INVALID_ARG, "q/kv_cache/out/o_part not 16-byte aligned");
-  const size_t xneed = xchg_need(dims, S, sms);
-  if (xchg == nullptr || !aligned16(xchg)) return fail(SMD_ERR_INVALID_ARG, "xchg is NULL or not 16-byte aligned");
-  if (xchg_bytes < xneed) return fail(SMD_ERR_WORKSPACE, "xchg %zu bytes < required %zu", xchg_bytes, xneed);
-  const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
-  smd::AttnParams a{};
-  a.q = q;
-  a.cache = kv_cache;
-  a.gidx = gidx;
-  a.sink = sink;
-  a.out = out;
-  a.lse = lse;
-  a.o_part = S > 1 ? o_part : nullptr;
-  a.lse_part = S > 1 ? lse_part : nullptr;
-  a.status = reinterpret_cast<uint32_t*>(status);
-  a.xchg = static_cast<uint8_t*>(xchg);
-  a.scale = scale;
-  a.num_pages = dims->num_pages;
-  a.T = dims->num_tokens;
-  a.H = dims->num_heads;
-  a.N = (int32_t)N;
-  a.P = dims->block_size;
-  a.S = S;
-  a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
-  if (a.tiles_per_split < 1) a.tiles_per_split = 1;
-  a.G = smd::attn_pairs((int64_t)a.T * S, sms);
+  const smd::AttnParams a = attn_params(dims, S, sms, q, kv_cache, gidx, sink, scale, out, lse, o_part, lse_part,
+                                        reinterpret_cast<uint32_t*>(status));
   const cudaError_t e = smd::launch_attn(a, stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "attention launch");
 }

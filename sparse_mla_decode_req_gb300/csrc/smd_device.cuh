@@ -1,11 +1,11 @@
-// Device-side building blocks for libsmd (sm_103a): the fp8_ds_mla row format, the
-// row dequantiser, and thin inline-PTX wrappers for mbarrier, tcgen05 (TMEM
-// allocation, MMA, loads/stores, fences) and the UMMA descriptors.
+// Device-side building blocks for libsmd (sm_103a): the fp8_ds_mla row format, the row
+// dequantiser shared by the attention kernel and the gather export, and thin inline-PTX
+// wrappers for mbarrier, TMA, tcgen05 (TMEM allocation, MMA, loads/stores, fences) and
+// the UMMA descriptors.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace smd {
@@ -16,10 +16,11 @@ namespace smd {
 constexpr int kLatent = 512;
 constexpr int kNope = 448;
 constexpr int kRope = 64;
-constexpr int kGroup = 64;
 constexpr int kDataBytes = 576;
 constexpr int kScaleBytes = 8;
 constexpr int kRowBytes = kDataBytes + kScaleBytes;
+constexpr int kNopePieces = kNope / 16;    // 28 pieces of 16 fp8 bytes
+constexpr int kRowPieces = kDataBytes / 16;  // 36 pieces of 16 bytes per data row
 
 struct CacheView {
   const uint8_t* base;
@@ -61,12 +62,7 @@ __device__ __forceinline__ const uint8_t* row_scales(const CacheView& c, int32_t
   return c.base + (int64_t)page * c.page_bytes + c.scale_start + (int64_t)off * kScaleBytes;
 }
 
-// 2^(code-127) as an fp32 bit pattern; code 0 is the subnormal 2^-127 and code 255
-// becomes +inf, which the scrub below turns into 0 for every element it scales.
-__device__ __forceinline__ float ue8m0_to_float(uint32_t code) {
-  return code == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(code << 23);
-}
-
+// ---------------------------------------------------------------- dequantisation
 // Zero every bf16 lane whose exponent field is all ones (inf or NaN).
 __device__ __forceinline__ uint32_t scrub_bf16x2(uint32_t v) {
   const uint32_t t = v & 0x7F807F80u;
@@ -74,51 +70,11 @@ __device__ __forceinline__ uint32_t scrub_bf16x2(uint32_t v) {
   const uint32_t bad_hi = (t >> 16) == 0x7F80u ? 0xFFFF0000u : 0u;
   return v & ~(bad_lo | bad_hi);
 }
-
-__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
-  return *reinterpret_cast<uint32_t*>(&v);
+__device__ __forceinline__ uint4 scrub_bf16x8(uint4 v) {
+  return make_uint4(scrub_bf16x2(v.x), scrub_bf16x2(v.y), scrub_bf16x2(v.z), scrub_bf16x2(v.w));
 }
 
-// Magnitudes at or above this fp32 value round to infinity in bf16 (halfway between the
-// largest finite bf16, 0x1.fep127, and 2^128); NaN compares false.
-constexpr uint32_t kBf16OverflowBits = 0x7F7F8000u;
-
-// Two e4m3 bytes (low byte = lower element) times a power-of-two scale -> scrubbed bf16x2.
-// fp8 -> fp16 is exact for every e4m3 value (hardware cvt, NaN stays NaN); the fp32
-// product is exact unless it overflows; the bf16 rounding is exact whenever the product
-// stays in bf16's normal range, so the result equals the exactly-rounded latent value.
-// Non-finite products and products that would round to infinity become 0.
-__device__ __forceinline__ uint32_t dequant_fp8x2(uint32_t two, float scale) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h2) : "r"(two));
-  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-  const float2 f = __half22float2(hv);
-  const float lim = __uint_as_float(kBf16OverflowBits);
-  float a = f.x * scale, b = f.y * scale;
-  a = fabsf(a) < lim ? a : 0.f;
-  b = fabsf(b) < lim ? b : 0.f;
-  return bf16x2_bits(__floats2bfloat162_rn(a, b));
-}
-
-// 16 fp8 bytes (uint4) -> 16 bf16 (two uint4), one scale for all.
-__device__ __forceinline__ void dequant16(const uint4 in, float scale, uint4& lo, uint4& hi) {
-  lo.x = dequant_fp8x2(in.x & 0xFFFFu, scale);
-  lo.y = dequant_fp8x2(in.x >> 16, scale);
-  lo.z = dequant_fp8x2(in.y & 0xFFFFu, scale);
-  lo.w = dequant_fp8x2(in.y >> 16, scale);
-  hi.x = dequant_fp8x2(in.z & 0xFFFFu, scale);
-  hi.y = dequant_fp8x2(in.z >> 16, scale);
-  hi.z = dequant_fp8x2(in.w & 0xFFFFu, scale);
-  hi.w = dequant_fp8x2(in.w >> 16, scale);
-}
-
-// Dequantisation without conversion instructions (which run at a quarter of the ALU
-// rate).  Placing an e4m3 byte s.eeee.mmm into bf16 bits as s.0000eeee.mmm0000 gives a
-// bf16 whose value times 2^120 is exactly the e4m3 value, for normal and subnormal
-// encodings alike (2^(e-127)(1+m/8) * 2^120 = 2^(e-7)(1+m/8);  m*2^-129 * 2^120 = m*2^-9).
-// The power-of-two scale is then one more exact bf16 multiply (rounded to nearest only
-// where the true product leaves bf16's range, like the fp32 route).  NaN bytes
-// (s.1111.111) are zeroed first; products that are not finite are zeroed after.
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
 // Zero the bytes of w that encode e4m3 NaN (low 7 bits all ones).  Adding one to each
 // byte's low 7 bits sets its bit 7 exactly for those bytes (no carry leaves a byte); a
@@ -129,127 +85,69 @@ __device__ __forceinline__ uint32_t zero_fp8_nans(uint32_t w) {
   asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(mask) : "r"(hit));
   return w & ~mask;
 }
-// Two bytes (selected by `sel` for __byte_perm) -> two bf16 carrying value / 2^120.
-__device__ __forceinline__ uint32_t fp8x2_to_bf16x2_bits(uint32_t w, uint32_t sel) {
-  const uint32_t y = __byte_perm(w, 0u, sel);             // 0x00bb00aa
-  return ((y & 0x007F007Fu) << 4) | ((y & 0x00800080u) << 8);
+
+// Dequantisation without conversion instructions.  Placing an e4m3 byte s.eeee.mmm into
+// bf16 bits as s.0000eeee.mmm0000 gives a bf16 whose value times 2^120 is exactly the
+// e4m3 value, for normal and subnormal encodings alike (2^(e-127)(1+m/8) * 2^120 =
+// 2^(e-7)(1+m/8); m*2^-129 * 2^120 = m*2^-9).  `sel` picks two bytes of w into the low
+// bytes of the two 16-bit halves (0x4140: bytes 0 and 1; 0x4342: bytes 2 and 3).
+__device__ __forceinline__ uint32_t place_fp8x2(uint32_t w, uint32_t sel) {
+  const uint32_t y = __byte_perm(w, 0u, sel);  // 0x00bb00aa
+  return ((y << 4) & 0x07F007F0u) | ((y << 8) & 0x80008000u);
 }
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-// 16 e4m3 bytes times 2^(code-127) -> 16 bf16 (two uint4), non-finite results zeroed.
-__device__ __forceinline__ void dequant16_fast(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
-  constexpr uint32_t k2p120 = 0x7B807B80u;  // bf16x2 (2^120, 2^120)
-  const uint32_t sb = code == 0 ? 0x0040u : (code << 7);  // bf16 2^(code-127); 255 -> inf
-  const uint32_t sc = sb | (sb << 16);
-  const bool scrub = code >= 247u;                          // only these codes can overflow
-  uint32_t w[4] = {zero_fp8_nans(in.x), zero_fp8_nans(in.y), zero_fp8_nans(in.z), zero_fp8_nans(in.w)};
-  uint32_t r[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    r[2 * i] = mul_bf16x2(mul_bf16x2(fp8x2_to_bf16x2_bits(w[i], 0x4140u), k2p120), sc);
-    r[2 * i + 1] = mul_bf16x2(mul_bf16x2(fp8x2_to_bf16x2_bits(w[i], 0x4342u), k2p120), sc);
-  }
-  if (scrub) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = scrub_bf16x2(r[i]);
-  }
-  lo = make_uint4(r[0], r[1], r[2], r[3]);
-  hi = make_uint4(r[4], r[5], r[6], r[7]);
-}
 
-// Attention-stage dequantisation: the same values as dequant16_fast, with the elements of
-// every group of four dims stored in the order (d0, d2, d1, d3) -- the order in which
-// they fall out of placing the four bytes of a 32-bit word in two bf16x2 words.  The
-// attention kernel stores Q in the same order, so Q.K is unchanged, and it restores the
-// order of O.  Fast path (warp-uniform): no NaN byte and code <= 134, so that one exact
-// multiply by 2^(code - 7) carries both the 2^120 of the placement and the scale.
-__device__ __forceinline__ void place4(uint32_t w, uint32_t& d02, uint32_t& d13) {
-  d02 = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
-  d13 = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
-}
-// True when the 16 bytes hold no NaN encoding (low 7 bits all ones).
-__device__ __forceinline__ bool fp8x16_no_nan(uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t hit = 0;
+// One 16-byte NoPE piece: 16 e4m3 bytes times 2^(code-127) -> 16 bf16 in element order
+// (lo = elements 0..7, hi = 8..15).  NaN bytes become 0; so does every product that is
+// not finite in bf16 (code 255 decodes to a NaN scale; codes >= 247 can overflow).
+//   code <= 134: one exact multiply by 2^(code-7) carries both the 2^120 of the
+//     placement and the scale, rounded once (exact unless the product leaves bf16's
+//     range at the bottom);
+//   code > 134: 2^120 first (exact), then the scale, then the non-finite scrub.
+// Both routes round the same exact product once, so they agree wherever both apply.
+// NaN bytes are rare: one test of all 16 bytes decides whether they are zeroed.
+__device__ __forceinline__ void dequant_piece(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
+  uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  const uint32_t nan_hit = (((w[0] & 0x7F7F7F7Fu) + 0x01010101u) | ((w[1] & 0x7F7F7F7Fu) + 0x01010101u) |
+                            ((w[2] & 0x7F7F7F7Fu) + 0x01010101u) | ((w[3] & 0x7F7F7F7Fu) + 0x01010101u)) &
+                           0x80808080u;
+  if (nan_hit != 0u) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) hit |= (w[i] & 0x7F7F7F7Fu) + 0x01010101u;
-  return (hit & 0x80808080u) == 0u;
-}
-__device__ __forceinline__ void dequant16_perm_fast(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
-  const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
-  const uint32_t sc = sb | (sb << 16);
-  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-  uint32_t r[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t a, b;
-    place4(w[i], a, b);
-    r[2 * i] = mul_bf16x2(a, sc);
-    r[2 * i + 1] = mul_bf16x2(b, sc);
+    for (int i = 0; i < 4; ++i) w[i] = zero_fp8_nans(w[i]);
   }
-  lo = make_uint4(r[0], r[1], r[2], r[3]);
-  hi = make_uint4(r[4], r[5], r[6], r[7]);
-}
-// The fast path for any bytes: NaN encodings are zeroed first (as the exact path does),
-// so it is exact whenever code <= 134.  A row that is not `valid` gets a zero multiplier
-// instead, so its 16 values come out as +0 or -0.
-__device__ __forceinline__ void dequant16_perm_nz(uint4 in, uint32_t code, bool valid, uint4& lo, uint4& hi) {
-  const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
-  const uint32_t sc = valid ? (sb | (sb << 16)) : 0u;
-  const uint32_t w[4] = {zero_fp8_nans(in.x), zero_fp8_nans(in.y), zero_fp8_nans(in.z), zero_fp8_nans(in.w)};
   uint32_t r[8];
+  if (code <= 134u) {
+    const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
+    const uint32_t sc = sb | (sb << 16);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t a, b;
-    place4(w[i], a, b);
-    r[2 * i] = mul_bf16x2(a, sc);
-    r[2 * i + 1] = mul_bf16x2(b, sc);
-  }
-  lo = make_uint4(r[0], r[1], r[2], r[3]);
-  hi = make_uint4(r[4], r[5], r[6], r[7]);
-}
-// Any input (NaN bytes, large or NaN codes): the exact path, then the same reordering.
-__device__ __forceinline__ void dequant16_perm_exact(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
-  dequant16_fast(in, code, lo, hi);
-  const uint32_t a0 = __byte_perm(lo.x, lo.y, 0x5410u), a1 = __byte_perm(lo.x, lo.y, 0x7632u);
-  const uint32_t a2 = __byte_perm(lo.z, lo.w, 0x5410u), a3 = __byte_perm(lo.z, lo.w, 0x7632u);
-  const uint32_t b0 = __byte_perm(hi.x, hi.y, 0x5410u), b1 = __byte_perm(hi.x, hi.y, 0x7632u);
-  const uint32_t b2 = __byte_perm(hi.z, hi.w, 0x5410u), b3 = __byte_perm(hi.z, hi.w, 0x7632u);
-  lo = make_uint4(a0, a1, a2, a3);
-  hi = make_uint4(b0, b1, b2, b3);
-}
-
-__device__ __forceinline__ uint4 scrub_bf16x8(uint4 v) {
-  v.x = scrub_bf16x2(v.x);
-  v.y = scrub_bf16x2(v.y);
-  v.z = scrub_bf16x2(v.z);
-  v.w = scrub_bf16x2(v.w);
-  return v;
-}
-
-// 16-byte global load; ALIGN16 = false splits it into two 8-byte loads (pages with an
-// odd slot count leave data rows only 8-byte aligned).
-template <bool ALIGN16>
-__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
-  if constexpr (ALIGN16) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
+    for (int i = 0; i < 4; ++i) {
+      r[2 * i] = mul_bf16x2(place_fp8x2(w[i], 0x4140u), sc);
+      r[2 * i + 1] = mul_bf16x2(place_fp8x2(w[i], 0x4342u), sc);
+    }
   } else {
-    const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
-    const uint2 b = __ldg(reinterpret_cast<const uint2*>(p + 8));
-    return make_uint4(a.x, a.y, b.x, b.y);
+    constexpr uint32_t k2p120 = 0x7B807B80u;        // bf16x2 (2^120, 2^120)
+    const uint32_t sb = code << 7;                  // bf16 2^(code - 127); 255 -> inf
+    const uint32_t sc = sb | (sb << 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r[2 * i] = scrub_bf16x2(mul_bf16x2(mul_bf16x2(place_fp8x2(w[i], 0x4140u), k2p120), sc));
+      r[2 * i + 1] = scrub_bf16x2(mul_bf16x2(mul_bf16x2(place_fp8x2(w[i], 0x4342u), k2p120), sc));
+    }
   }
+  lo = make_uint4(r[0], r[1], r[2], r[3]);
+  hi = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
+// ---------------------------------------------------------------- global loads
 // Loads through the read-only path as volatile PTX: the compiler keeps them in program
 // order and cannot sink them to their first use, so a batch of them is in flight at once.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 __device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
@@ -257,23 +155,15 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
   asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint32_t ldg_nc_u8(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
 __device__ __forceinline__ int32_t ldg_nc_s32(const void* p) {
   int32_t v;
   asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
+// 16 bytes; ALIGN16 = false splits them into two 8-byte loads (pages with an odd slot
+// count leave data rows only 8-byte aligned).
 template <bool ALIGN16>
-__device__ __forceinline__ uint4 ldg16_early(const uint8_t* p) {
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
   if constexpr (ALIGN16) {
     return ldg_nc_v4(p);
   } else {
@@ -290,14 +180,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------- misc PTX
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // ---------------------------------------------------------------- dependent launches
@@ -310,9 +209,7 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 // try_wait with a suspend-time hint: a waiting thread sleeps until the phase completes or
 // about 0.1 ms passes, instead of spinning on the issue slots its neighbours need.
 constexpr uint32_t kSuspendHintNs = 100000;
@@ -327,20 +224,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// try_wait with a caller-chosen suspend-time hint (ns).
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-// Non-blocking probe of a phase (no suspend): true once the phase with `parity` completed.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+// Non-blocking probe of a phase: true once the phase with `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -360,47 +245,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
   return true;
 }
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared-memory location in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior writes.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 // Per-warpgroup register budget changes (all four warps of a warpgroup execute them).
@@ -411,6 +260,22 @@ __device__ __forceinline__ void regs_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------- TMA
+// 2-D tiled tensor load into shared memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Prefetch of the same 2-D box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -425,16 +290,10 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 // Generic-proxy shared-memory writes -> visible to the async proxy (UMMA operand reads).
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, f32 accumulate).
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -446,52 +305,66 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16.  A (M=128) sits in TMEM with lane m =
-// row m and each 32-bit column holding two consecutive K elements (lower element in the
-// low half), so one K=16 step reads 8 columns.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// The same, issued by one elected lane of a converged warp.  The whole warp runs the issue
+// loop, so its descriptor arithmetic stays warp-uniform (uniform registers) and, unrolled
+// with constant offsets, an MMA issues at the tensor core's pace (a loop run by one
+// divergent lane with per-iteration descriptor math took ~90 cycles per MMA on GB300).
+__device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
 // Arrive (once) on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-
+// The same commit from one elected lane of a converged warp (the lane that issued the MMAs
+// with umma_ss_elect: elect.sync picks the same lane for the same member mask).
+__device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w reads lanes 32w..32w+31).
+#define SMD_R32_OUT(r)                                                                                           \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),    \
+      "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),     \
+      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),    \
+      "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define SMD_R32_IN(r)                                                                                             \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),   \
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), \
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), \
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+#define SMD_R32_LIST                                                                                          \
+  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27," \
+  "%28,%29,%30,%31}"
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w reads lanes
+// 32(w%4)..32(w%4)+31, thread i lane 32(w%4)+i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-        "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " SMD_R32_LIST ", [%32];" : SMD_R32_OUT(r) : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%32], " SMD_R32_LIST ";" ::SMD_R32_IN(r), "r"(taddr)
+               : "memory");
+}
+// 16 lanes of the warp's TMEM quarter, twice: threads 0-15 read lanes base+0..15 at
+// columns [c, c+32), threads 16-31 the same lanes at columns [c+32, c+64).  This is the
+// access pattern of an M=64 accumulator, whose rows sit in lanes 0-15 of each quarter.
+__device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x32.b32 " SMD_R32_LIST ", [%32], 32;"
+               : SMD_R32_OUT(r)
+               : "r"(taddr));
 }
 
 // UMMA shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
@@ -521,7 +394,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled slab
 // whose rows are 128 bytes apart (8-row atoms of 1024 bytes).
-__device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
+__host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 

@@ -37,6 +37,7 @@ struct CombineParams {
   void* out;              // bf16 [T, H, 512]
   float* lse;             // [T, H] or null
   int32_t T, S, H;
+  int32_t sms;            // SMs of the device (sizes the grid to one wave)
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
@@ -50,19 +51,21 @@ struct AttnParams {
   float* o_part;          // [T, S, H, 512]            (S > 1)
   float* lse_part;        // [T, S, H]                 (S > 1)
   uint32_t* status;       // device status word
-  uint8_t* xchg;          // partial-score exchange buffers, attn_xchg_bytes(G) bytes
   float scale;
   int64_t num_pages;
   int32_t T, H, N, P, S;
   int32_t tiles_per_split;
-  int32_t G;              // CTA pairs launched; pair c takes work items c, c + G, ...
+  int32_t HG;             // head groups of 64 (CTAs per token and split)
+  int32_t G;              // CTAs launched; CTA c takes work items c, c + G, ...
+  uint64_t wait_limit_ns; // bound of every pipeline wait inside the kernel
 };
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
-int attn_ctas_per_split();
-// CTA pairs the attention kernel launches for `items` (token, split) work items on a
-// device with `sms` SMs, and the exchange-buffer bytes that many pairs need.
-int attn_pairs(int64_t items, int sms);
-size_t attn_xchg_bytes(int pairs);
+// CTAs that share one (token, split): one per group of 64 heads.
+int attn_ctas_per_split(int H);
+// CTAs the attention kernel launches for `items` work items on a device with `sms` SMs.
+int attn_ctas(int64_t items, int sms);
+// Bound of the kernels' pipeline waits (a test hook can shorten it), default 2 s.
+uint64_t wait_limit_ns();
 
 // Sets the thread-local message returned by smd_last_error() and returns `code`.
 int set_error(int code, const char* fmt, ...);

@@ -56,8 +56,9 @@ def test_split_selector_rules(lib):
     # long context, low batch: the selector uses many splits to fill the GPU
     s4 = api.select_num_splits(_dims(), 32, 152)
     assert 8 <= s4 <= 32
-    # the workloads' automatic choices: single request 4 (the short-work cap), batch 32
-    # at 2048 entries 2, batch 4 at 2176 entries 17 (one CTA wave, two tiles per split)
+    # the workloads' automatic choices: single request 4 (the short-work cap), batch 32 x
+    # 128 heads at 2048 entries 2 (128 CTAs, one wave), batch 4 x 128 heads at 2176
+    # entries 17 (136 CTAs, one wave, two tiles per split)
     assert api.select_num_splits(_dims(T=1, H=64, K=512, W=128), 8, 152) == 4
     assert api.select_num_splits(_dims(T=32, H=128, K=2048, W=0), 0, 152) == 2
     assert api.select_num_splits(_dims(T=4, H=128, K=2048, W=128), 32, 152) == 17
@@ -75,27 +76,15 @@ def test_split_selector_rules(lib):
     assert api.select_num_splits(_dims(), 0, 152) == api.select_num_splits(_dims(), 0, 152)
 
 
-XCHG_PER_CTA = 2 * 256 * 32 * 4   # two buffers x 256 softmax threads x 32 fp32 partial scores
-
-
-def _xchg(items, sms):
-    pairs = min(items, sms // 2) if items > 0 else 1
-    return pairs * 2 * XCHG_PER_CTA
-
-
 def test_workspace_size_layout(lib):
+    up = lambda x: (x + 255) // 256 * 256
     d = _dims(T=4, H=128, K=2048, W=128)
     s = api.select_num_splits(d, -8, 152)
-    n = api.workspace_size(d, -8, 152)
     T, N, H = 4, 2176, 128
-    need = 256 + T * N * 4 + T * s * H * 512 * 4 + T * s * H * 4 + _xchg(T * s, 152)
-    assert need <= n <= need + 4 * 256
-    assert api.attention_xchg_size(d, -8, 152) == _xchg(T * s, 152)
+    assert api.workspace_size(d, -8, 152) == 256 + up(T * N * 4) + up(T * s * H * 512 * 4) + up(T * s * H * 4)
+    # one split: the status word and the converted slots only
     d1 = _dims(T=256, H=64, K=512, W=128)
-    up = lambda x: (x + 255) // 256 * 256
-    assert api.workspace_size(d1, 1, 152) == 256 + up(256 * 640 * 4) + up(_xchg(256, 152))
-    # the exchange scratch is bounded by the SM count, not by the batch
-    assert api.attention_xchg_size(d1, 1, 152) == api.attention_xchg_size(_dims(T=4096, H=64, K=512, W=128), 1, 152)
+    assert api.workspace_size(d1, 1, 152) == 256 + up(256 * 640 * 4)
 
 
 @pytest.mark.parametrize("field,value", [("num_heads", 0), ("num_heads", 129), ("block_size", 0),
@@ -154,11 +143,11 @@ def test_gather_and_attention_host_checks(lib):
     assert lib.smd_gather_dequant(ctypes.byref(d), None, None, 0, None, None) == api.SMD_OK
     ad = api.attention_dims(2, 64, 640, 100)
     rc = lib.smd_sparse_mla_attention(ctypes.byref(ad), al, al, al, None, ctypes.c_float(1.0), -33, al, None,
-                                      None, None, None, al, ctypes.c_size_t(1 << 20), None)
+                                      None, None, None, None)
     assert rc == api.SMD_ERR_INVALID_ARG and "num_splits" in api.last_error()
     ad0 = api.attention_dims(0, 64, 640, 100)
     assert lib.smd_sparse_mla_attention(ctypes.byref(ad0), None, None, None, None, ctypes.c_float(1.0), 0, None,
-                                        None, None, None, None, None, ctypes.c_size_t(0), None) == api.SMD_OK
+                                        None, None, None, None, None) == api.SMD_OK
 
 
 def test_version(lib):
