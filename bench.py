@@ -8,8 +8,10 @@ L2 is flushed (a 512 MiB write) between timed steps, outside the per-step CUDA e
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
 
---config picks one of the five decode workloads (0 tiny, 1 single request [default],
-2 mid batch, 3 large batch, 4 long context).  Under torchrun each rank runs its own
+--config picks the headline workload among the five decode shapes (0 tiny, 1 single
+request, 2 mid batch, 3 large batch [default: the largest single-GPU step], 4 long
+context); --extra-configs lists the others measured in the same run and reported under
+``extra_workloads``.  Each step is one CUDA-graph replay of the smd_sparse_mla_decode call.  Under torchrun each rank runs its own
 replica of the workload on its own GPU (weak scaling, no data-path collective); the
 timed region is bracketed by barriers and the max time over ranks is reported.
 ``--impl reference`` times the float64 CPU oracle on the host cores instead.
@@ -38,9 +40,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--extra-configs", default="2,4,1", help="other workloads measured in the same run")
+    ap.add_argument("--extra-steps", type=int, default=300)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample length")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -224,13 +228,156 @@ def workload_config(w, splits):
             "splits": splits, "l2": "flushed between timed steps (512 MiB write)"}
 
 
+# The benchmark spec's roofline: max(gathered bytes / 8 TB/s, FLOPs / dense bf16 tensor peak),
+# with the GB300 spec figures (the measured peaks are the `roofline` object's denominators).
+SPEC_HBM_GBS = 8000.0
+SPEC_BF16_TFLOPS = 2250.0
+
+
+def step_bytes(inp, S: int) -> dict:
+    """Bytes one decode step must move (algorithmic): the gathered 584-byte rows, q read, out
+    written, lse written, the index lists, request ids and block table read.  The converted
+    slots and split partials are the implementation's own traffic and are listed apart."""
+    w = inp.workload
+    T, H, N = w.num_tokens, w.num_heads, w.n_entries
+    gathered = 584 * inp.n_valid
+    qo = 2 * T * H * 512 * 2
+    lse = T * H * 4
+    idx = T * N * 4 + T * 4 + inp.block_table.numel() * 4
+    impl = 2 * T * N * 4 + ((T * S * H * 512 * 4 + T * S * H * 4) * 2 if S > 1 else 0)
+    return {"gathered": gathered, "full": gathered + qo + lse + idx, "q_and_out": qo, "lse": lse, "indices": idx,
+            "implementation_scratch": impl}
+
+
+def fractions(H: int, rows: int, nbytes: dict, seconds: float, peaks: dict) -> dict:
+    """Roofline fractions of `seconds` for one step's work."""
+    flops = 4.0 * 512 * H * rows
+    t_ns = max(nbytes["gathered"] / (SPEC_HBM_GBS * 1e9), flops / (SPEC_BF16_TFLOPS * 1e12))
+    t_meas = max(nbytes["gathered"] / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    t_full = nbytes["full"] / (peaks["hbm_gbs"] * 1e9)
+    return {"north_star_frac": t_ns / seconds, "north_star_roofline_us": t_ns * 1e6,
+            "measured_peak_frac": t_meas / seconds, "full_bytes_frac": t_full / seconds,
+            "full_bytes_floor_us": t_full * 1e6, "full_bytes_gbs": nbytes["full"] / seconds / 1e9}
+
+
+def measure(api, lib, synth, torch, w, seed, dev, flush, K: int, W: int, KP: int, sampler=None, pg=None):
+    """Times one workload: K CUDA-graph replays of the product call smd_sparse_mla_decode (L2
+    flushed between them, events around each replay), then KP staged steps with events
+    between the three kernels for the per-kernel breakdown and the attention roofline."""
+    import ctypes
+
+    inp = synth.make_inputs(w, seed=seed, device=dev)
+    T, H, N = w.num_tokens, w.num_heads, w.n_entries
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    topk = inp.topk_idx if w.topk else None
+    swa = inp.swa_idx if w.swa else None
+    dims = api.make_dims(inp.q, inp.kv_cache, inp.block_table, inp.req_id, topk, swa, w.block_size)
+    S = api.select_num_splits(dims, w.max_splits, sms)
+    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws = torch.zeros(api.workspace_size(dims, w.max_splits, sms), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def call():
+        api.sparse_mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.req_id, topk, swa, inp.sink, inp.scale,
+                              out=out, lse=lse, num_splits=w.max_splits, workspace=ws, block_size=w.block_size,
+                              stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()  # per-device set-up outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+        for _ in range(max(W, 3)):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if sampler is not None:
+            sampler.start()
+            time.sleep(0.1)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if pg is not None:
+            pg.barrier()
+        clocks = sampler.stop() if sampler is not None else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    status = api.read_status(ws)  # raises on a recorded timeout
+
+    # staged pass: convert | attention | combine with events between them
+    gidx = torch.empty(T, N, dtype=torch.int32, device=dev)
+    o_part = torch.empty(T, S, H, 512, dtype=torch.float32, device=dev) if S > 1 else None
+    lse_part = torch.empty(T, S, H, dtype=torch.float32, device=dev) if S > 1 else None
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    P = api._ptr
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    conv_args = (ctypes.byref(dims), P(inp.block_table), P(inp.req_id), P(topk), P(swa), P(gidx), sp)
+    attn_dims = api.attention_dims(T, H, N, inp.num_pages, w.block_size)
+    attn_args = (ctypes.byref(attn_dims), P(inp.q), P(inp.kv_cache), P(gidx), P(inp.sink),
+                 ctypes.c_float(inp.scale), int(w.max_splits), P(out), P(lse), P(o_part), P(lse_part), P(st), sp)
+    comb_args = (T, S, H, P(o_part), P(lse_part), P(inp.sink), P(out), P(lse), sp)
+    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KP)]
+    with torch.cuda.stream(stream):
+        for i in range(KP + 3):
+            flush.zero_()
+            e = evk[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            api._check(lib.smd_convert_req_index(*conv_args))
+            if e:
+                e[1].record(stream)
+            api._check(lib.smd_sparse_mla_attention(*attn_args))
+            if e:
+                e[2].record(stream)
+            if S > 1:
+                api._check(lib.smd_lse_combine(*comb_args))
+            if e:
+                e[3].record(stream)
+        torch.cuda.synchronize()
+    assert int(st.item()) == 0, "a kernel's bounded wait gave up during the benchmark"
+    return {"inp": inp, "S": S, "step_ms": step_ms, "wall": wall, "clocks": clocks, "status": status,
+            "attn_ms": [e[1].elapsed_time(e[2]) for e in evk], "conv_ms": [e[0].elapsed_time(e[1]) for e in evk],
+            "comb_ms": [e[2].elapsed_time(e[3]) for e in evk], "out": out, "stream": stream}
+
+
+def summary(w, r, peaks, src) -> dict:
+    """Per-workload numbers shared by the headline and the extra workloads."""
+    inp, S = r["inp"], r["S"]
+    rows = inp.n_valid
+    nb = step_bytes(inp, S)
+    mean_s = statistics.mean(r["step_ms"]) / 1e3
+    med_s = statistics.median(r["step_ms"]) / 1e3
+    attn_s = statistics.mean(r["attn_ms"]) / 1e3
+    roof = roofline(w.num_heads, rows, attn_s, peaks, src, load_traffic(w.name))
+    roof["kernel"] = "smd::attn_kernel"
+    roof["launch_us_mean"] = attn_s * 1e6
+    roof.update({k: v for k, v in fractions(w.num_heads, rows, nb, attn_s, peaks).items()})
+    return {
+        "workload": w.name, "splits": S, "valid_rows": rows, "bytes_per_step": nb,
+        "step_us_mean": mean_s * 1e6, "step_us_median": med_s * 1e6,
+        "step_us_p90": sorted(r["step_ms"])[int(0.9 * (len(r["step_ms"]) - 1))] * 1e3,
+        "rows_per_s": rows / mean_s, "roofline_attention": roof,
+        "roofline_step": fractions(w.num_heads, rows, nb, med_s, peaks),
+        "kernels_us_mean": {"convert": statistics.mean(r["conv_ms"]) * 1e3, "attention": attn_s * 1e6,
+                            "combine": statistics.mean(r["comb_ms"]) * 1e3 if S > 1 else 0.0},
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
-
-    import ctypes
 
     import torch
 
@@ -244,110 +391,45 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     lib = api.load()
-    w = synth.WORKLOADS[args.config]
-    seed = rank_seed(args.config, rank)
-    inp = synth.make_inputs(w, seed=seed, device=dev)
-    T, H, N = w.num_tokens, w.num_heads, w.n_entries
-    rows_per_step = inp.n_valid
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    dims = api.make_dims(inp.q, inp.kv_cache, inp.block_table, inp.req_id,
-                         inp.topk_idx if w.topk else None, inp.swa_idx if w.swa else None, w.block_size)
-    S = api.select_num_splits(dims, w.max_splits, sms)
-    topk = inp.topk_idx if w.topk else None
-    swa = inp.swa_idx if w.swa else None
-
-    # buffers of the staged step
-    gidx = torch.empty(T, N, dtype=torch.int32, device=dev)
-    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
-    o_part = torch.empty(T, S, H, 512, dtype=torch.float32, device=dev) if S > 1 else None
-    lse_part = torch.empty(T, S, H, dtype=torch.float32, device=dev) if S > 1 else None
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sp = ctypes.c_void_p(stream.cuda_stream)
-    P = api._ptr
-    conv_args = (ctypes.byref(dims), P(inp.block_table), P(inp.req_id), P(topk), P(swa), P(gidx), sp)
-    attn_dims = api.attention_dims(T, H, N, inp.num_pages, w.block_size)
-    attn_args = (ctypes.byref(attn_dims), P(inp.q), P(inp.kv_cache), P(gidx), P(inp.sink),
-                 ctypes.c_float(inp.scale), int(w.max_splits), P(out), P(lse), P(o_part), P(lse_part),
-                 P(status), sp)
-    comb_args = (T, S, H, P(o_part), P(lse_part), P(inp.sink), P(out), P(lse), sp)
-
-    def step():
-        api._check(lib.smd_convert_req_index(*conv_args))
-        api._check(lib.smd_sparse_mla_attention(*attn_args))
-        if S > 1:
-            api._check(lib.smd_lse_combine(*comb_args))
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-
-    K = args.steps
-    # Timed region: events bracket whole steps only, so the step's kernels keep their
-    # programmatic launch overlap (an event between two kernels would serialise them).
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.1)
-    if pg is not None:
-        pg.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush.zero_()
-        e = ev[i]
-        e[0].record(stream)
-        step()
-        e[1].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if pg is not None:
-        pg.barrier()
-    clocks = sampler.stop()
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    # Per-kernel durations (the roofline's attention launch and the breakdown): a second
-    # pass of the same steps with events between the kernels, still L2-flushed.
-    KP = min(K, 200)
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KP)]
-    for i in range(KP):
-        flush.zero_()
-        e = evk[i]
-        e[0].record(stream)
-        api._check(lib.smd_convert_req_index(*conv_args))
-        e[1].record(stream)
-        api._check(lib.smd_sparse_mla_attention(*attn_args))
-        e[2].record(stream)
-        if S > 1:
-            api._check(lib.smd_lse_combine(*comb_args))
-        e[3].record(stream)
-    torch.cuda.synchronize()
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evk]
-    conv_ms = [e[0].elapsed_time(e[1]) for e in evk]
-    comb_ms = [e[2].elapsed_time(e[3]) for e in evk]
-    total_s = max_over_ranks(pg, sum(step_ms) / 1e3, dev)
-    assert int(status.item()) == 0, "a kernel's bounded wait gave up during the benchmark"
-    value = job_rate(rows_per_step, K, world, total_s)
-    ms_per_step = total_s / K * 1e3
-
     peaks, src = load_peaks()
-    traffic = load_traffic(w.name)
-    roof = roofline(H, rows_per_step, statistics.mean(attn_ms) / 1e3, peaks, src, traffic)
-    roof["kernel"] = "smd::attn_pair_kernel"
-    roof["launch_ms_mean"] = statistics.mean(attn_ms)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    w = synth.WORKLOADS[args.config]
+    K = args.steps
+    sampler = ClockSampler(local)
+    r = measure(api, lib, synth, torch, w, rank_seed(args.config, rank), dev, flush, K, args.warmup,
+                min(K, 200), sampler, pg)
+    inp, S = r["inp"], r["S"]
+    rows_per_step = inp.n_valid
+    total_s = max_over_ranks(pg, sum(r["step_ms"]) / 1e3, dev)
+    value = job_rate(rows_per_step, K, world, total_s)
+    head = summary(w, r, peaks, src)
+    roof = {k: head["roofline_attention"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof.update({k: v for k, v in head["roofline_attention"].items() if k not in roof})
 
     # end to end through the public call with host buffers: h2d of the step's inputs,
     # decode, d2h of out + lse, per step (out still holds the device path's result)
     try:
-        e2e = run_e2e(api, inp, w, dev, stream, flush, min(args.e2e_steps, K), rows_per_step, device_out=out)
+        e2e = run_e2e(api, inp, w, dev, r["stream"], flush, min(args.e2e_steps, K), rows_per_step,
+                      device_out=r["out"])
     except Exception as exc:  # keep the device-timed line; the failure is reported in it
         e2e = {"seconds": None, "steps": 0, "h2d": 0, "d2h": 0, "error": repr(exc)[:300]}
         print(f"e2e leg failed: {exc!r}", file=sys.stderr)
-    # every rank joins the reduction (a failed leg contributes +inf, which voids the value)
     secs = max_over_ranks(pg, e2e["seconds"] if e2e["seconds"] is not None else float("inf"), dev)
     e2e_val = job_rate(rows_per_step, e2e["steps"], world, secs) if secs != float("inf") else None
+
+    # the other target workloads (mid batch, long context; the single-request latency case)
+    # measured the same way in the same run, on rank 0's replica only
+    extras = {}
+    if rank == 0 and world == 1 and args.extra_configs:
+        for ci in [int(x) for x in args.extra_configs.split(",") if x.strip() != ""]:
+            if ci == args.config:
+                continue
+            we = synth.WORKLOADS[ci]
+            re_ = measure(api, lib, synth, torch, we, rank_seed(ci, 0), dev, flush, args.extra_steps, 3,
+                          min(args.extra_steps, 200))
+            extras[we.name] = summary(we, re_, peaks, src)
+            del re_
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -356,24 +438,30 @@ def main(argv=None):
                "sample": f"{steps_done} oracle steps of one token each ({rows_done} valid rows, {el:.1f} s, "
                          f"numpy BLAS on all host cores)"}
 
+    S_launches = 2 + (1 if S > 1 else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": total_s / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded; fp8_ds_mla rows quantised from N(0,1))",
         "config": workload_config(w, S),
         "roofline": roof,
-        "step_breakdown_ms": {"convert": statistics.mean(conv_ms), "attention": statistics.mean(attn_ms),
-                              "combine": statistics.mean(comb_ms) if S > 1 else 0.0,
-                              "timing": f"second pass of {KP} steps with events between the kernels "
-                                        "(no launch overlap); the step time above keeps it"},
-        "hbm_gbs_step": 584.0 * rows_per_step / (ms_per_step / 1e3) / 1e9,
+        "roofline_step": head["roofline_step"],
+        "bytes_per_step": head["bytes_per_step"],
+        "step_timing": {"us_mean": head["step_us_mean"], "us_median": head["step_us_median"],
+                        "us_p90": head["step_us_p90"],
+                        "method": "CUDA-graph replay of the smd_sparse_mla_decode call (convert, attention, "
+                                  "combine), events around each replay, 512 MiB L2 flush between replays"},
+        "step_breakdown_us": {**head["kernels_us_mean"],
+                              "timing": f"{min(K, 200)} staged steps with events between the kernels "
+                                        "(no launch overlap)"},
+        "extra_workloads": extras,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e["steps"], "transfers": "one h2d of the packed inputs, one d2h of out + lse",
                 "matches_device_path": e2e.get("matches_device_path"), **({"error": e2e["error"]} if "error" in e2e else {})},
-        "gpu_launches": K * (2 + (1 if S > 1 else 0)),
-        "clocks": clocks,
-        "wall_s_timed_region": wall,
+        "gpu_launches": K * S_launches,
+        "clocks": r["clocks"],
+        "wall_s_timed_region": r["wall"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -458,19 +546,20 @@ def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step, device_out=No
         api.sparse_mla_decode(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
                               dbuf.get("topk_idx"), dbuf.get("swa_idx"), inp.sink, inp.scale,
                               out=res["out"], lse=res["lse"], num_splits=w.max_splits, workspace=ws,
-                              block_size=w.block_size)
+                              block_size=w.block_size, stream=stream)
         h_res.copy_(d_res, non_blocking=True)
 
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in evs:
-        flush.zero_()
-        a.record(stream)
-        one()
-        b.record(stream)
-    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):  # every copy, call and event on one stream
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            one()
+            b.record(stream)
+        torch.cuda.synchronize()
     secs = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     r = {"seconds": secs, "steps": steps, "h2d": nb_in, "d2h": nb_out}
     if device_out is not None:  # same inputs, same kernels: the results must agree bit for bit
