@@ -332,6 +332,7 @@ struct Converter {
   struct Raw {
     uint4 v[2][9];  // v[h][st]: piece 4st + m of row 8h + ((st + q) & 7) of the warp's 16
     uint2 sc;       // lane i < 16: scale row of row i
+    int64_t roff;   // lane i < 16: byte offset of row i's data in the cache
     uint32_t ok;    // bit i: row i is valid (same in every lane)
   };
   // Issues the read of the tile's converted slot of row 16 w + lane (lanes 0-15; -1 when
@@ -354,6 +355,7 @@ struct Converter {
       d.sc = ldg_nc_v2(cv.base + (int64_t)page * cv.page_bytes + cv.scale_start + (int64_t)o * kScaleBytes);
     }
     const int64_t row_off = (int64_t)page * cv.page_bytes + (int64_t)o * kDataBytes;  // lanes 0-15: row i
+    d.roff = row_off;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -364,25 +366,49 @@ struct Converter {
         if ((d.ok >> ri) & 1u) d.v[h][st] = ldg16<ALIGN16>(cv.base + off + st * 64 + m * 16);
       }
   }
-  __device__ void store(uint32_t stage, int w, const Raw& d) const {
+  // Straight-line conversion of every piece on the fast path (no NaN byte, code <= 134),
+  // so the unrolled steps interleave and each piece's registers die once it is stored;
+  // the rare pieces outside that case are read again (an L1/L2 hit) and redone on the
+  // exact path afterwards, overwriting their fast result.
+  __device__ void store(const AttnParams& p, uint8_t* stage, int w, const Raw& d) const {
+    uint32_t redo = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t row0 = kRowsPerConvWarp * w + 8 * h;
 #pragma unroll
       for (int st = 0; st < 7; ++st) {  // NoPE: slab st, chunks 2m and 2m + 1
         const uint32_t ri = (st + q) & 7;
-        const uint32_t rbase = stage + st * kSlab + (row0 + ri) * 128;
         const uint32_t wv = __shfl_sync(0xffffffffu, st < 4 ? d.sc.x : d.sc.y, 8 * h + ri);
+        const uint32_t code = (wv >> (8 * (st & 3))) & 0xFFu;  // code st of the row
+        uint8_t* rb = stage + st * kSlab + (row0 + ri) * 128;
         uint4 lo, hi;
-        dequant_piece(d.v[h][st], (wv >> (8 * (st & 3))) & 0xFFu, lo, hi);
-        st_shared_v4(rbase + (((2 * m) ^ ri) << 4), lo);
-        st_shared_v4(rbase + (((2 * m + 1) ^ ri) << 4), hi);
+        dequant_fast(d.v[h][st], code, lo, hi);
+        redo |= needs_exact(d.v[h][st], code) ? 1u << (7 * h + st) : 0u;
+        *reinterpret_cast<uint4*>(rb + (((2 * m) ^ ri) << 4)) = lo;
+        *reinterpret_cast<uint4*>(rb + (((2 * m + 1) ^ ri) << 4)) = hi;
       }
 #pragma unroll
       for (int st = 7; st < 9; ++st) {  // RoPE: slab 7, chunk 4(st - 7) + m
         const uint32_t ri = (st + q) & 7;
-        st_shared_v4(stage + 7 * kSlab + (row0 + ri) * 128 + (((4 * (st - 7) + m) ^ ri) << 4),
-                     scrub_bf16x8(d.v[h][st]));
+        *reinterpret_cast<uint4*>(stage + 7 * kSlab + (row0 + ri) * 128 + (((4 * (st - 7) + m) ^ ri) << 4)) =
+            scrub_bf16x8(d.v[h][st]);
+      }
+    }
+    if (__any_sync(0xffffffffu, redo != 0u)) {  // rare: NaN bytes or codes above 134
+#pragma unroll 1
+      for (int i = 0; i < 14; ++i) {
+        const int h = i / 7, st = i - 7 * h;
+        const uint32_t ri = (st + q) & 7;
+        const int64_t off = __shfl_sync(0xffffffffu, d.roff, 8 * h + ri);
+        const uint32_t wv = __shfl_sync(0xffffffffu, st < 4 ? d.sc.x : d.sc.y, 8 * h + ri);
+        if ((redo >> i) & 1u) {
+          const uint4 raw = ldg16<ALIGN16>(p.cache + off + st * 64 + m * 16);
+          uint4 lo, hi;
+          dequant_piece(raw, (wv >> (8 * (st & 3))) & 0xFFu, lo, hi);
+          uint8_t* rb = stage + st * kSlab + (kRowsPerConvWarp * w + 8 * h + ri) * 128;
+          *reinterpret_cast<uint4*>(rb + (((2 * m) ^ ri) << 4)) = lo;
+          *reinterpret_cast<uint4*>(rb + (((2 * m + 1) ^ ri) << 4)) = hi;
+        }
       }
     }
   }
@@ -396,7 +422,7 @@ __device__ void converter_warps(uint8_t* smem, Misc* m, const AttnParams& p, int
   const Converter<ALIGN16> cv(lane);
   const int g = cw / kConvGroupWarps, w = cw % kConvGroupWarps;
   const uint64_t limit = p.wait_limit_ns;
-  const uint32_t stage = smem_u32(smem + kOffStage + g * kStageBytes);
+  uint8_t* stage = smem + kOffStage + g * kStageBytes;
   typename Converter<ALIGN16>::Raw d;
   TileCursor c;  // the tile whose slots are read next (this group's tiles only)
   c.init(p, cid);
@@ -418,7 +444,7 @@ __device__ void converter_warps(uint8_t* smem, Misc* m, const AttnParams& p, int
       if (lane == 0) record_abort(m, p.status);
       return;
     }
-    cv.store(stage, w, d);
+    cv.store(p, stage, w, d);
     if (lane < kRowsPerConvWarp) m->valid[g][kRowsPerConvWarp * w + lane] = (d.ok >> lane) & 1u;
     fence_async_smem();
     warp_arrive(&m->kfull[g]);
@@ -579,27 +605,42 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
     if (!(ok = wait_warp(&m->erdv, nerdv & 1, m, limit))) break;
     ++nerdv;
     tc_fence_after();
+    // O^T (lane = latent dim, column = head) leaves through a warp-private 4 KB slice of
+    // the P^T buffers (free once O is final): per block of 128 dims and 32 heads the warp
+    // writes its 32 dim-lanes of the 32 heads as fp32 rows [head][32 dims], then reads them
+    // back as 16-byte pieces (lanes 8r..8r+7: head row r) and stores 4 consecutive dims of
+    // one head per lane, so a warp store covers whole row segments (64 B of bf16 or 128 B
+    // of fp32 per head) instead of 2 or 4 bytes in each of 32 rows.
     const int hvalid = min(kHeads, p.H - it.g * kHeads);
     const int64_t row_base = p.S == 1 ? (int64_t)it.t * p.H + it.g * kHeads
                                       : ((int64_t)it.t * p.S + it.split) * p.H + it.g * kHeads;
+    float* stg = reinterpret_cast<float*>(smem + kOffP) + warp * 1024;  // [32 heads][32 dims] fp32
 #pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
+      const int blk = cc >> 1, h0 = 32 * (cc & 1);
       uint32_t o[32];
       tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
       tmem_wait_ld();
-      const int d = 128 * (cc >> 1) + 32 * warp + lane;  // latent dim of this lane
-      const int h0 = 32 * (cc & 1);
-      if (p.S == 1) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + row_base * kLatent + d;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (h0 + i < hvalid) dst[(int64_t)(h0 + i) * kLatent] = __float2bfloat16_rn(__uint_as_float(o[i]) * m->factor[fb][h0 + i]);
-      } else {
-        float* dst = p.o_part + row_base * kLatent + d;
+      for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __uint_as_float(o[i]);
+      __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (h0 + i < hvalid) dst[(int64_t)(h0 + i) * kLatent] = __uint_as_float(o[i]) * m->factor[fb][h0 + i];
+      for (int k = 0; k < 8; ++k) {
+        const int hr = 4 * k + (lane >> 3), dd = 4 * (lane & 7);  // head row, first of 4 dims
+        const float4 v = *reinterpret_cast<const float4*>(stg + hr * 32 + dd);
+        const float f = m->factor[fb][h0 + hr];
+        if (h0 + hr < hvalid) {
+          const int64_t off = (row_base + h0 + hr) * kLatent + blk * 128 + 32 * warp + dd;
+          if (p.S == 1) {
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off) =
+                make_uint2(bf16x2_bits(__floats2bfloat162_rn(v.x * f, v.y * f)),
+                           bf16x2_bits(__floats2bfloat162_rn(v.z * f, v.w * f)));
+          } else {
+            *reinterpret_cast<float4*>(p.o_part + off) = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
+          }
+        }
       }
+      __syncwarp();  // the rows are read before the next block overwrites them
     }
     tc_fence_before();
     warp_arrive(&m->ofree);  // the next item's first PV may overwrite O^T

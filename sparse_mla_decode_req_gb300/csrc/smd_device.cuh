@@ -104,39 +104,47 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 // One 16-byte NoPE piece: 16 e4m3 bytes times 2^(code-127) -> 16 bf16 in element order
 // (lo = elements 0..7, hi = 8..15).  NaN bytes become 0; so does every product that is
 // not finite in bf16 (code 255 decodes to a NaN scale; codes >= 247 can overflow).
-//   code <= 134: one exact multiply by 2^(code-7) carries both the 2^120 of the
-//     placement and the scale, rounded once (exact unless the product leaves bf16's
-//     range at the bottom);
-//   code > 134: 2^120 first (exact), then the scale, then the non-finite scrub.
-// Both routes round the same exact product once, so they agree wherever both apply.
-// NaN bytes are rare: one test of all 16 bytes decides whether they are zeroed.
-__device__ __forceinline__ void dequant_piece(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
-  uint32_t w[4] = {in.x, in.y, in.z, in.w};
-  const uint32_t nan_hit = (((w[0] & 0x7F7F7F7Fu) + 0x01010101u) | ((w[1] & 0x7F7F7F7Fu) + 0x01010101u) |
-                            ((w[2] & 0x7F7F7F7Fu) + 0x01010101u) | ((w[3] & 0x7F7F7F7Fu) + 0x01010101u)) &
-                           0x80808080u;
-  if (nan_hit != 0u) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = zero_fp8_nans(w[i]);
-  }
+//
+// dequant_fast handles the common case without a branch: no NaN byte and code <= 134,
+// where one exact multiply by 2^(code-7) carries both the 2^120 of the placement and the
+// scale, rounded once (exact unless the product leaves bf16's range at the bottom).
+// needs_exact tells whether a piece is outside that case; dequant_piece handles any
+// piece: NaN bytes zeroed, then for code > 134 2^120 first (exact), then the scale, then
+// the non-finite scrub.  Both routes round the same exact product once, so they agree
+// wherever both apply.
+__device__ __forceinline__ bool needs_exact(uint4 in, uint32_t code) {
+  const uint32_t hit = (((in.x & 0x7F7F7F7Fu) + 0x01010101u) | ((in.y & 0x7F7F7F7Fu) + 0x01010101u) |
+                        ((in.z & 0x7F7F7F7Fu) + 0x01010101u) | ((in.w & 0x7F7F7F7Fu) + 0x01010101u)) &
+                       0x80808080u;
+  return hit != 0u || code > 134u;
+}
+__device__ __forceinline__ void dequant_fast(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
+  const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
+  const uint32_t sc = sb | (sb << 16);
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
   uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    r[2 * i] = mul_bf16x2(place_fp8x2(w[i], 0x4140u), sc);
+    r[2 * i + 1] = mul_bf16x2(place_fp8x2(w[i], 0x4342u), sc);
+  }
+  lo = make_uint4(r[0], r[1], r[2], r[3]);
+  hi = make_uint4(r[4], r[5], r[6], r[7]);
+}
+__device__ __forceinline__ void dequant_piece(uint4 in, uint32_t code, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {zero_fp8_nans(in.x), zero_fp8_nans(in.y), zero_fp8_nans(in.z), zero_fp8_nans(in.w)};
   if (code <= 134u) {
-    const uint32_t sb = (code + 120u) << 7;  // bf16 2^(code - 7)
-    const uint32_t sc = sb | (sb << 16);
+    dequant_fast(make_uint4(w[0], w[1], w[2], w[3]), code, lo, hi);
+    return;
+  }
+  constexpr uint32_t k2p120 = 0x7B807B80u;        // bf16x2 (2^120, 2^120)
+  const uint32_t sb = code << 7;                  // bf16 2^(code - 127); 255 -> inf
+  const uint32_t sc = sb | (sb << 16);
+  uint32_t r[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      r[2 * i] = mul_bf16x2(place_fp8x2(w[i], 0x4140u), sc);
-      r[2 * i + 1] = mul_bf16x2(place_fp8x2(w[i], 0x4342u), sc);
-    }
-  } else {
-    constexpr uint32_t k2p120 = 0x7B807B80u;        // bf16x2 (2^120, 2^120)
-    const uint32_t sb = code << 7;                  // bf16 2^(code - 127); 255 -> inf
-    const uint32_t sc = sb | (sb << 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      r[2 * i] = scrub_bf16x2(mul_bf16x2(mul_bf16x2(place_fp8x2(w[i], 0x4140u), k2p120), sc));
-      r[2 * i + 1] = scrub_bf16x2(mul_bf16x2(mul_bf16x2(place_fp8x2(w[i], 0x4342u), k2p120), sc));
-    }
+  for (int i = 0; i < 4; ++i) {
+    r[2 * i] = scrub_bf16x2(mul_bf16x2(mul_bf16x2(place_fp8x2(w[i], 0x4140u), k2p120), sc));
+    r[2 * i + 1] = scrub_bf16x2(mul_bf16x2(mul_bf16x2(place_fp8x2(w[i], 0x4342u), k2p120), sc));
   }
   lo = make_uint4(r[0], r[1], r[2], r[3]);
   hi = make_uint4(r[4], r[5], r[6], r[7]);
