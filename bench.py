@@ -323,7 +323,7 @@ def measure(api, lib, synth, torch, w, seed, dev, flush, K: int, W: int, KP: int
     sp = ctypes.c_void_p(stream.cuda_stream)
     conv_args = (ctypes.byref(dims), P(inp.block_table), P(inp.req_id), P(topk), P(swa), P(gidx), sp)
     attn_dims = api.attention_dims(T, H, N, inp.num_pages, w.block_size)
-    attn_args = (ctypes.byref(attn_dims), P(inp.q), P(inp.kv_cache), P(gidx), P(inp.sink),
+    attn_args = (ctypes.byref(attn_dims), None, P(inp.q), P(inp.kv_cache), P(gidx), None, P(inp.sink),
                  ctypes.c_float(inp.scale), int(w.max_splits), P(out), P(lse), P(o_part), P(lse_part), P(st), sp)
     comb_args = (T, S, H, P(o_part), P(lse_part), P(inp.sink), P(out), P(lse), sp)
     evk = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KP)]

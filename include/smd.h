@@ -1,6 +1,6 @@
 /*
- * smd.h -- C ABI of libsmd: sparse MLA decode over an fp8_ds_mla paged latent cache,
- * hand-written CUDA for NVIDIA GB300 (sm_103a).
+ * smd.h -- C ABI of libsmd: sparse MLA decode over a paged latent cache (fp8_ds_mla or
+ * bf16 rows), hand-written CUDA for NVIDIA GB300 (sm_103a).
  *
  * One decode step, per query token t (one token per request), computes
  *
@@ -19,14 +19,25 @@
  *   5. a log-sum-exp combine of split partials that also adds the per-head sink logit
  *      to the softmax denominator (same report, test symbol _launch_sparse_decode_reduce).
  *
- * Cache format.  A page of P = block_size slots is P * 584 bytes: first the P data rows
- * of 576 bytes (448 fp8 e4m3 NoPE values, then 64 little-endian bf16 RoPE values), then
- * the P scale rows of 8 bytes (7 UE8M0 codes, one per 64 NoPE values, then one pad
- * byte).  Global slot g lives in page g / P at offset g % P.  Latent element d < 448 is
- * e4m3(byte d) * 2^(code[d/64] - 127); element 448 + r is RoPE value r.  An element
- * that is not finite once held as bf16 (NaN byte, code 255, non-finite RoPE, overflow)
- * is replaced by 0: the cache is never trusted to be NaN-free (vLLM PR #52212 report,
- * "实现拆解" item 3).
+ * Cache formats (smd_dims.cache_format).  Global slot g lives in page g / P at offset
+ * g % P, P = block_size.
+ *   SMD_CACHE_FP8_DS_MLA (0): a page is P * 584 bytes: first the P data rows of 576
+ *     bytes (448 fp8 e4m3 NoPE values, then 64 little-endian bf16 RoPE values), then the
+ *     P scale rows of 8 bytes (7 UE8M0 codes, one per 64 NoPE values, then one pad
+ *     byte).  Latent element d < 448 is e4m3(byte d) * 2^(code[d/64] - 127); element
+ *     448 + r is RoPE value r.
+ *   SMD_CACHE_BF16 (1): a page is P * 1024 bytes, one row of 512 little-endian bf16
+ *     latent values (NoPE then RoPE) per slot (vLLM PR #41217 report, the bf16-KV decode
+ *     path _forward_bf16_kv; the pages print no layout, this is the plainest reading).
+ * An element that is not finite once held as bf16 (NaN byte, code 255, non-finite bf16,
+ * overflow) is replaced by 0: the cache is never trusted to be NaN-free (vLLM PR #52212
+ * report, "实现拆解" item 3).
+ *
+ * Two scopes.  The top-k entries (the main scope) and the sliding-window entries attend
+ * in one softmax.  By default both live in kv_cache under one block table; with
+ * smd_decode_opts.swa_kv_cache the window entries live in a second cache of the same
+ * format with its own block table, page size and page count (vLLM PR #52212 report,
+ * "实现拆解" items 1 and 3: main and SWA scopes over the compressed and window caches).
  *
  * Semantics (float64 definition, up to bf16/fp32 rounding):
  *   s[h,e]  = scale * q[t,h,:] . k_e              over the valid entries e of token t
@@ -72,8 +83,11 @@ enum {
   SMD_ERR_DEVICE_CHECK = -6
 };
 
+enum { SMD_CACHE_FP8_DS_MLA = 0, SMD_CACHE_BF16 = 1 };
+
 #define SMD_LATENT_DIM 512
-#define SMD_ROW_BYTES 584
+#define SMD_ROW_BYTES 584      /* fp8_ds_mla bytes per slot */
+#define SMD_ROW_BYTES_BF16 1024
 #define SMD_MAX_HEADS 128
 #define SMD_MAX_SPLITS 32
 
@@ -87,11 +101,44 @@ typedef struct smd_dims {
   int32_t block_size;          /* P >= 1: slots per page (64 for the DSV4 cache)         */
   int32_t topk;                /* K >= 0: top-k entries per token                       */
   int32_t swa;                 /* W >= 0: sliding-window entries per token              */
-  int32_t pad_;                /* reserved, set to 0                                    */
+  int32_t cache_format;        /* SMD_CACHE_FP8_DS_MLA (0) or SMD_CACHE_BF16 (1)         */
   int64_t bt_stride;           /* >= max_blocks_per_req: block_table row stride         */
   int64_t topk_stride;         /* >= topk: topk_idx row stride                          */
   int64_t swa_stride;          /* >= swa: swa_idx row stride                            */
 } smd_dims;
+
+/*
+ * Optional parts of a decode step (a NULL smd_decode_opts* means all off).  A zeroed
+ * struct is "all off" too.
+ *   swa_kv_cache     the window scope's own cache (format dims->cache_format), or NULL:
+ *                    the window entries then use kv_cache, block_table and dims' P
+ *   swa_block_table  i32 [R, swa_bt_stride]: its block table.  The decode takes both or
+ *                    neither; the conversion reads only the block table (and the window
+ *                    paging fields), the attention only the cache (swa_num_pages,
+ *                    swa_block_size)
+ *   swa_num_pages, swa_block_size, swa_max_blocks_per_req, swa_bt_stride: as in smd_dims,
+ *                    for the window cache (num_pages * block_size < 2^31)
+ *   topk_length      i32 [T] or NULL: top-k column k of token t is masked when
+ *                    k >= topk_length[t] (SGLang PR #26208 report, "关键源码片段",
+ *                    _gather_dequant_dsv4_kernel's HAS_TOPK_LENGTH branch; one query
+ *                    token per sequence)
+ *   compact          nonzero: the conversion packs each token's valid slots to the front
+ *                    of its row and writes per-token counts, and the attention reads no
+ *                    masked row (vLLM PR #41217 report, "实现拆解" item 2: sparse lengths
+ *                    built before the decode).  Same results; fewer rows gathered when
+ *                    many entries are masked.
+ */
+typedef struct smd_decode_opts {
+  const uint8_t *swa_kv_cache;
+  const int32_t *swa_block_table;
+  int64_t swa_num_pages;
+  int64_t swa_bt_stride;
+  int32_t swa_block_size;
+  int32_t swa_max_blocks_per_req;
+  const int32_t *topk_length;
+  int32_t compact;
+  int32_t reserved_;           /* set to 0 */
+} smd_decode_opts;
 
 /*
  * Split selector (host only, no device call unless num_sms <= 0).  Returns the number of
@@ -109,11 +156,11 @@ typedef struct smd_dims {
 SMD_API int smd_select_num_splits(const smd_dims *dims, int num_splits, int num_sms);
 
 /*
- * Device workspace bytes smd_sparse_mla_decode needs for the given split request
+ * Device workspace bytes smd_sparse_mla_decode(_ex) needs for the given split request
  * (same num_splits/num_sms meaning as smd_select_num_splits): a 256-byte status word,
- * the converted indices [T, K+W] int32 and, when S > 1, the split partials o_part f32
- * [T, S, H, 512] and lse_part f32 [T, S, H], each 256-byte aligned.  Returns 0 on bad
- * dims.
+ * the converted indices [T, K+W] int32, the per-token counts [T, 2] int32 and, when
+ * S > 1, the split partials o_part f32 [T, S, H, 512] and lse_part f32 [T, S, H], each
+ * 256-byte aligned.  Returns 0 on bad dims.
  */
 SMD_API size_t smd_workspace_size(const smd_dims *dims, int num_splits, int num_sms);
 
@@ -121,7 +168,7 @@ SMD_API size_t smd_workspace_size(const smd_dims *dims, int num_splits, int num_
  * The whole decode step (conversion, fused gather + dequant + tcgen05 attention, and
  * the LSE combine when S > 1).
  *   q           bf16 [T, H, 512], row-major, the latent order [NoPE 448 | RoPE 64]
- *   kv_cache    u8   [num_pages, block_size * 584] (format above)
+ *   kv_cache    u8   [num_pages, block_size * row bytes] (format above)
  *   block_table i32  [R, bt_stride]: page of block b of request r, -1 = unused
  *   req_id      i32  [T]: request of token t
  *   topk_idx    i32  [T, topk_stride] request-local positions, -1 = none (NULL iff K=0)
@@ -142,11 +189,23 @@ SMD_API int smd_sparse_mla_decode(const smd_dims *dims, const void *q, const uin
                                   int num_splits, void *workspace, size_t workspace_bytes,
                                   smd_stream_t stream);
 
+/* smd_sparse_mla_decode with the optional parts of smd_decode_opts (NULL = none). */
+SMD_API int smd_sparse_mla_decode_ex(const smd_dims *dims, const smd_decode_opts *opts, const void *q,
+                                     const uint8_t *kv_cache, const int32_t *block_table,
+                                     const int32_t *req_id, const int32_t *topk_idx,
+                                     const int32_t *swa_idx, const float *sink, float scale, void *out,
+                                     float *lse, int num_splits, void *workspace,
+                                     size_t workspace_bytes, smd_stream_t stream);
+
 /*
  * Steps 2-4 alone, for already-converted slots: the fused gather + dequant + tcgen05
- * attention kernel over gidx i32 [T, K+W] as written by smd_convert_req_index (entries
- * < 0 or >= num_pages * block_size are masked).  The split count S follows num_splits as
- * for smd_select_num_splits (current device's SM count).  S == 1: writes out bf16
+ * attention kernel over gidx i32 [T, K+W] as written by smd_convert_req_index(_ex)
+ * (entries < 0 or beyond their cache are masked).  counts (i32 [T, 2] or NULL) are that
+ * conversion's per-token counts: token t then attends to its first counts[t, 1] entries,
+ * the first counts[t, 0] of them in the main scope; without counts the first K entries
+ * are the main scope and the rest the window scope.  Of opts only the window cache
+ * (swa_kv_cache, swa_num_pages, swa_block_size) is read.  The split count S follows
+ * num_splits as for smd_select_num_splits (current device's SM count).  S == 1: writes out bf16
  * [T, H, 512] and lse f32 [T, H] (lse may be NULL) with the sink in the denominator.
  * S > 1: writes each split's normalised output o_part f32 [T, S, H, 512] and its
  * sink-free lse_part f32 [T, S, H] (-inf for a split without valid entries), to be
@@ -154,10 +213,10 @@ SMD_API int smd_sparse_mla_decode(const smd_dims *dims, const void *q, const uin
  * gets bit 0 set if a bounded wait inside the kernel gives up.  dims->topk + dims->swa
  * is the row length of gidx; the index pointers of dims are not used.
  */
-SMD_API int smd_sparse_mla_attention(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
-                                     const int32_t *gidx, const float *sink, float scale, int num_splits,
-                                     void *out, float *lse, float *o_part, float *lse_part,
-                                     int32_t *status, smd_stream_t stream);
+SMD_API int smd_sparse_mla_attention(const smd_dims *dims, const smd_decode_opts *opts, const void *q,
+                                     const uint8_t *kv_cache, const int32_t *gidx, const int32_t *counts,
+                                     const float *sink, float scale, int num_splits, void *out, float *lse,
+                                     float *o_part, float *lse_part, int32_t *status, smd_stream_t stream);
 
 /*
  * Step 1 alone: writes gidx i32 [T, K+W] (top-k entries first, window entries at
@@ -170,10 +229,39 @@ SMD_API int smd_convert_req_index(const smd_dims *dims, const int32_t *block_tab
                                   const int32_t *swa_idx, int32_t *gidx, smd_stream_t stream);
 
 /*
+ * smd_convert_req_index with the options: window entries through opts->swa_block_table
+ * and the window paging fields when that table is non-NULL (-1 past swa_num_pages), top-k
+ * columns cut at topk_length[t], and with opts->compact
+ * each token's valid slots packed to the front of its gidx row in column order (the rest
+ * of the row is left as it was) and counts i32 [T, 2] = (valid top-k entries, valid
+ * entries) written; counts is required with compact and ignored without it.
+ */
+SMD_API int smd_convert_req_index_ex(const smd_dims *dims, const smd_decode_opts *opts,
+                                     const int32_t *block_table, const int32_t *req_id,
+                                     const int32_t *topk_idx, const int32_t *swa_idx, int32_t *gidx,
+                                     int32_t *counts, smd_stream_t stream);
+
+/*
+ * The pages' ragged conversion (vLLM PR #41217 report, "关键源码片段",
+ * _convert_req_index_to_global_index_kernel): token t writes out[cu_seqlens[t] + j] for
+ * j in [0, cu_seqlens[t+1] - cu_seqlens[t]) from column j of token_indices
+ * i32 [T, ti_stride]: block_table[req_id[t], i / P] * P + i % P, or 0 (the pages' fill)
+ * when i < 0 or i / P >= max_blocks_per_req.  Like the pages' kernel it does not check
+ * the physical page; a request id outside [0, num_requests) and a position j >= num_cols
+ * (past the index array's columns) also give 0.  cu_seqlens i32 [T + 1] is
+ * non-decreasing from 0 and out holds cu_seqlens[T] entries.  Only num_tokens,
+ * num_requests, max_blocks_per_req, block_size and bt_stride of dims are read.
+ */
+SMD_API int smd_convert_req_index_ragged(const smd_dims *dims, const int32_t *block_table,
+                                         const int32_t *req_id, const int32_t *token_indices,
+                                         int32_t num_cols, int64_t ti_stride, const int32_t *cu_seqlens,
+                                         int32_t *out, smd_stream_t stream);
+
+/*
  * Step 2 alone (a test and debugging export): for each of num_rows global slots
  * gidx[i] writes the dequantised bf16 latent row kv_out[i, 0:512]; a slot that is
- * negative or >= num_pages * block_size gives a zero row.  Only dims->num_pages and
- * dims->block_size are read.
+ * negative or >= num_pages * block_size gives a zero row.  Only dims->num_pages,
+ * dims->block_size and dims->cache_format are read.
  */
 SMD_API int smd_gather_dequant(const smd_dims *dims, const uint8_t *kv_cache, const int32_t *gidx,
                                int64_t num_rows, void *kv_out, smd_stream_t stream);
@@ -193,8 +281,11 @@ SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_
 
 /*
  * Reads the device status word at the start of a decode workspace into *device_status
- * after synchronising `stream`.  Returns SMD_ERR_TIMEOUT if a kernel recorded that a
- * bounded wait gave up, SMD_OK otherwise (or SMD_ERR_CUDA if the copy fails).
+ * after synchronising `stream`.  Bit 0: a kernel's bounded wait gave up; bit 1: a range
+ * check of a library built with SMD_DEBUG failed (that build re-checks the address of
+ * every gathered row, index read and output write against the buffer sizes and skips an
+ * access that fails).  Returns SMD_ERR_DEVICE_CHECK if bit 1 is set, else SMD_ERR_TIMEOUT
+ * if bit 0 is set, SMD_OK otherwise (or SMD_ERR_CUDA if the copy fails).
  */
 SMD_API int smd_read_status(const void *workspace, int32_t *device_status, smd_stream_t stream);
 
@@ -215,7 +306,9 @@ SMD_API int smd_read_status(const void *workspace, int32_t *device_status, smd_s
  * any stream capture.  All calls on a device share the one array and it keeps the last
  * call's contents (the call resets the status word itself and overwrites everything else
  * it reads), so calls whose kernels overlap on the GPU -- e.g. on two streams without an
- * ordering between them -- race on the scratch.  Serialise them.
+ * ordering between them -- race on the scratch.  Serialise them.  The cached address
+ * belongs to the device's primary context: after cudaDeviceReset it is stale, and this
+ * call must not be used again in that process.
  */
 #define SMD_STATIC_SCRATCH_BYTES (32u << 20)
 SMD_API int smd_sparse_mla_decode_static_scratch(const smd_dims *dims, const void *q, const uint8_t *kv_cache,
@@ -223,6 +316,14 @@ SMD_API int smd_sparse_mla_decode_static_scratch(const smd_dims *dims, const voi
                                                  const int32_t *topk_idx, const int32_t *swa_idx,
                                                  const float *sink, float scale, void *out, float *lse,
                                                  int num_splits, smd_stream_t stream);
+
+/*
+ * smd_read_status for the static scratch of the current device: the status word of the
+ * last smd_sparse_mla_decode_static_scratch call on it, after synchronising `stream`.
+ * Returns SMD_ERR_TIMEOUT if a bounded wait gave up, SMD_ERR_INVALID_ARG if no such call
+ * was made on this device yet.
+ */
+SMD_API int smd_read_static_scratch_status(int32_t *device_status, smd_stream_t stream);
 
 /*
  * Test and fault-injection hook (not part of the decode semantics): sets the bound, in

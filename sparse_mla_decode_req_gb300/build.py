@@ -2,7 +2,10 @@
 
 Each translation unit is compiled in parallel, then linked into one shared library
 with the CUDA runtime statically linked, so the library has no run-time dependency on a
-particular libcudart.  Usage: ``python -m sparse_mla_decode_req_gb300.build [--force]``.
+particular libcudart.  ``debug=True`` builds the range-checking variant libsmd_debug.so
+(SMD_DEBUG defined: every gathered row, index read and output write is re-checked against
+the buffer sizes, a failure sets bit 1 of the status word).
+Usage: ``python -m sparse_mla_decode_req_gb300.build [--force] [--debug]``.
 """
 from __future__ import annotations
 
@@ -18,6 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsmd.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libsmd_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           "-I", INCLUDE, "-I", CSRC]
@@ -41,18 +46,19 @@ def _stale(lib: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, debug: bool = False) -> str:
     srcs = sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "smd.h"))
-    if not force and not _stale(LIB, srcs + headers + [os.path.abspath(__file__)]):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and not _stale(lib, srcs + headers + [os.path.abspath(__file__)]):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DSMD_DEBUG"] if debug else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *COMMON, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -65,16 +71,16 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     args = sys.argv[1:]
     print(build(force="--force" in args, verbose="-v" in args,
-                extra=["-Xptxas", "-v"] if "--ptxas" in args else None))
+                extra=["-Xptxas", "-v"] if "--ptxas" in args else None, debug="--debug" in args))

@@ -113,19 +113,25 @@ __device__ __forceinline__ bool aborted(const Misc* m) {
 }
 __device__ __forceinline__ void record_abort(Misc* m, uint32_t* status) {
   atomicExch(&m->abort, 1u);
-  if (status != nullptr) atomicOr(status, 1u);
+  if (status != nullptr) atomicOr(status, kStatusTimeout);
 }
 
+// One probe of a phase: the suspending try_wait normally; a non-blocking test when the
+// bound is shorter than try_wait's suspend time (a bound that short is only set to make
+// the waits give up, and a suspending probe could outlast it by finding the phase done).
+__device__ __forceinline__ bool probe(uint64_t* bar, uint32_t parity, uint64_t limit) {
+  return limit < kSuspendHintNs ? mbar_test(bar, parity) : mbar_try_wait(bar, parity);
+}
 // Bounded wait that also gives up once another role of this CTA has aborted.
 __device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, const Misc* m, uint64_t limit) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!probe(bar, parity, limit)) {
     if (aborted(m) || globaltimer_ns() - t0 > limit) return false;
   }
   return true;
 }
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Misc* m, uint64_t limit) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (probe(bar, parity, limit)) return true;
   return wait_slow(bar, parity, m, limit);
 }
 // The same wait done by a whole warp, with a warp-uniform result, so that a warp never
@@ -142,9 +148,11 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
 }
 
 // One work item: (token t, split, head group g); tiles [tile_begin, tile_begin + n) of the
-// token's entries (n = 0 for a split past the end).
+// token's entries (n = 0 for a split past the end).  The token attends to its first ntot
+// converted entries, the first kmain of them in the main cache and the rest in the window
+// cache (the call's K and N, or the per-token counts of a compacted conversion).
 struct Item {
-  int t, split, g, tile_begin, n;
+  int t, split, g, tile_begin, n, kmain, ntot;
 };
 __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
   Item it;
@@ -153,7 +161,13 @@ __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
   it.t = ts / p.S;
   it.split = ts - it.t * p.S;
   it.tile_begin = it.split * p.tiles_per_split;
-  const int ntok = (p.N + kTile - 1) / kTile;
+  it.kmain = p.K;
+  it.ntot = p.N;
+  if (p.counts != nullptr) {
+    it.ntot = min(max(__ldg(p.counts + 2 * it.t + 1), 0), p.N);
+    it.kmain = min(max(__ldg(p.counts + 2 * it.t), 0), it.ntot);
+  }
+  const int ntok = (it.ntot + kTile - 1) / kTile;
   it.n = max(0, min(ntok, it.tile_begin + p.tiles_per_split) - it.tile_begin);
   return it;
 }
@@ -182,7 +196,9 @@ struct TileCursor {
   __device__ bool first() const { return k == 0; }
   __device__ bool last() const { return k == it.n - 1; }
   __device__ int64_t row0(const AttnParams& p) const { return (int64_t)it.t * p.N + (int64_t)(it.tile_begin + k) * kTile; }
-  __device__ int rows(const AttnParams& p) const { return min(kTile, p.N - (it.tile_begin + k) * kTile); }
+  __device__ int rows(const AttnParams& p) const { return min(kTile, it.ntot - (it.tile_begin + k) * kTile); }
+  // first entry index of the tile within the token's list
+  __device__ int entry0() const { return (it.tile_begin + k) * kTile; }
   __device__ void next(const AttnParams& p) {
     ++k;
     settle(p);
@@ -325,45 +341,62 @@ constexpr int kConvGroupWarps = kConvWarps / 2;
 constexpr int kRowsPerConvWarp = kTile / kConvGroupWarps;  // 16
 static_assert(kRowsPerConvWarp == 16, "two 8-row sets per converter warp");
 
+// A row's converted slot and the scope (cache) it lives in.
+struct SlotRef {
+  int32_t g;      // -1: masked or past the end
+  int32_t scope;  // 0: main cache, 1: window cache
+};
+__device__ __forceinline__ const CacheDesc& scope_cache(const AttnParams& p, int32_t scope) {
+  return scope ? p.cache2 : p.cache;
+}
+// Issues the read of the slot of entry row `r` of tile `c` (the value is validated where
+// it is used, so the read stays in flight meanwhile).
+__device__ __forceinline__ SlotRef read_slot(const AttnParams& p, const TileCursor& c, bool v, int r) {
+  SlotRef s{-1, 0};
+  if (v && r < c.rows(p) && in_range(c.row0(p) + r < (int64_t)p.T * p.N, p.status)) {
+    s.g = ldg_nc_s32(p.gidx + c.row0(p) + r);
+    s.scope = c.entry0() + r >= c.it.kmain ? 1 : 0;
+  }
+  return s;
+}
+
 template <bool ALIGN16>
 struct Converter {
   int lane, q, m;  // q = lane / 4: the row offset of this lane's segments; m = lane % 4: its piece
   __device__ Converter(int lane_) : lane(lane_), q(lane_ >> 2), m(lane_ & 3) {}
   struct Raw {
-    uint4 v[2][9];  // v[h][st]: piece 4st + m of row 8h + ((st + q) & 7) of the warp's 16
-    uint2 sc;       // lane i < 16: scale row of row i
-    int64_t roff;   // lane i < 16: byte offset of row i's data in the cache
-    uint32_t ok;    // bit i: row i is valid (same in every lane)
+    uint4 v[2][9];   // v[h][st]: piece 4st + m of row 8h + ((st + q) & 7) of the warp's 16
+    uint2 sc;        // lane i < 16: scale row of row i
+    uint64_t rptr;   // lane i < 16: address of row i's data
+    uint32_t ok;     // bit i: row i is valid (same in every lane)
   };
-  // Issues the read of the tile's converted slot of row 16 w + lane (lanes 0-15; -1 when
-  // the row is past the end).  The value is validated where it is used, so the read
-  // stays in flight meanwhile.
-  __device__ int32_t slot(const AttnParams& p, const TileCursor& c, bool v, int w) const {
-    const int r = kRowsPerConvWarp * w + lane;
-    int32_t g = -1;
-    if (v && lane < kRowsPerConvWarp && r < c.rows(p)) g = ldg_nc_s32(p.gidx + c.row0(p) + r);
-    return g;
+  __device__ SlotRef slot(const AttnParams& p, const TileCursor& c, bool v, int w) const {
+    return lane < kRowsPerConvWarp ? read_slot(p, c, v, kRowsPerConvWarp * w + lane) : SlotRef{-1, 0};
   }
-  __device__ void load(const AttnParams& p, int32_t sl, Raw& d) const {
-    const CacheView cv = make_cache_view(p.cache, p.P);
-    const bool mine = lane < kRowsPerConvWarp && sl >= 0 && (int64_t)sl < p.num_pages * p.P;
+  __device__ void load(const AttnParams& p, SlotRef sl, Raw& d) const {
+    const CacheDesc& cd = scope_cache(p, sl.scope);
+    const bool mine = lane < kRowsPerConvWarp && sl.g >= 0 && (int64_t)sl.g < cd.num_pages * cd.P;
     d.ok = __ballot_sync(0xffffffffu, mine) & 0xFFFFu;
     d.sc = make_uint2(0, 0);
-    int32_t page = 0, o = 0;
+    const uint8_t* row = cd.base;
     if (mine) {
-      slot_page_off(cv, sl, page, o);
-      d.sc = ldg_nc_v2(cv.base + (int64_t)page * cv.page_bytes + cv.scale_start + (int64_t)o * kScaleBytes);
+      const CacheView cv = make_cache_view(cd.base, cd.P);
+      int32_t page, o;
+      slot_page_off(cv, sl.g, page, o);
+      if (!in_range(page >= 0 && page < cd.num_pages && o >= 0 && o < cd.P, p.status)) page = o = 0;
+      const uint8_t* pg = cv.base + (int64_t)page * cv.page_bytes;
+      row = pg + (int64_t)o * kDataBytes;
+      d.sc = ldg_nc_v2(pg + cv.scale_start + (int64_t)o * kScaleBytes);
     }
-    const int64_t row_off = (int64_t)page * cv.page_bytes + (int64_t)o * kDataBytes;  // lanes 0-15: row i
-    d.roff = row_off;
+    d.rptr = reinterpret_cast<uint64_t>(row);
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int st = 0; st < 9; ++st) {
         const int ri = 8 * h + ((st + q) & 7);
-        const int64_t off = __shfl_sync(0xffffffffu, row_off, ri);
+        const uint64_t rp = __shfl_sync(0xffffffffu, d.rptr, ri);
         d.v[h][st] = make_uint4(0, 0, 0, 0);
-        if ((d.ok >> ri) & 1u) d.v[h][st] = ldg16<ALIGN16>(cv.base + off + st * 64 + m * 16);
+        if ((d.ok >> ri) & 1u) d.v[h][st] = ldg16<ALIGN16>(reinterpret_cast<const uint8_t*>(rp) + st * 64 + m * 16);
       }
   }
   // Straight-line conversion of every piece on the fast path (no NaN byte, code <= 134),
@@ -399,10 +432,10 @@ struct Converter {
       for (int i = 0; i < 14; ++i) {
         const int h = i / 7, st = i - 7 * h;
         const uint32_t ri = (st + q) & 7;
-        const int64_t off = __shfl_sync(0xffffffffu, d.roff, 8 * h + ri);
+        const uint64_t rp = __shfl_sync(0xffffffffu, d.rptr, 8 * h + ri);
         const uint32_t wv = __shfl_sync(0xffffffffu, st < 4 ? d.sc.x : d.sc.y, 8 * h + ri);
         if ((redo >> i) & 1u) {
-          const uint4 raw = ldg16<ALIGN16>(p.cache + off + st * 64 + m * 16);
+          const uint4 raw = ldg16<ALIGN16>(reinterpret_cast<const uint8_t*>(rp) + st * 64 + m * 16);
           uint4 lo, hi;
           dequant_piece(raw, (wv >> (8 * (st & 3))) & 0xFFu, lo, hi);
           uint8_t* rb = stage + st * kSlab + (kRowsPerConvWarp * w + 8 * h + ri) * 128;
@@ -431,11 +464,11 @@ __device__ void converter_warps(uint8_t* smem, Misc* m, const AttnParams& p, int
   };
   if (g == 1) skip();
   bool v0 = c.valid(p);
-  int32_t s0 = cv.slot(p, c, v0, w);
+  SlotRef s0 = cv.slot(p, c, v0, w);
   skip();
   skip();
   bool v1 = c.valid(p);
-  int32_t s1 = cv.slot(p, c, v1, w);
+  SlotRef s1 = cv.slot(p, c, v1, w);
   skip();
   skip();
   cv.load(p, s0, d);
@@ -459,6 +492,71 @@ __device__ void converter_warps(uint8_t* smem, Misc* m, const AttnParams& p, int
   }
 }
 
+// bf16 latent rows (1024 bytes: 512 little-endian bf16, NoPE then RoPE): nothing to
+// dequantise, only the non-finite elements to zero.  All eight converter warps take every
+// tile, warp cw owning rows 8cw .. 8cw+7, moved in 16 steps of one 64-byte segment per
+// row (step st = dims 32st .. 32st+31: slab st/2, chunks 4(st&1) .. +3), lanes 4i..4i+3
+// taking row (st + i) mod 8 as on the fp8 path.  A tile's rows stay in registers while the
+// warp waits for their stage, so the gathers of tile j + 1 are in flight during the
+// wait for the PV of tile j - 1.
+constexpr int kBf16RowBytes = 1024;
+__device__ void converter_warps_bf16(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int cw, int lane) {
+  const int q = lane >> 2, mm = lane & 3;
+  const uint64_t limit = p.wait_limit_ns;
+  uint4 v[16];
+  uint32_t ok = 0;
+  auto slot = [&](const TileCursor& c, bool valid) -> SlotRef {
+    return lane < 8 ? read_slot(p, c, valid, 8 * cw + lane) : SlotRef{-1, 0};
+  };
+  auto load = [&](SlotRef sl) {
+    const CacheDesc& cd = scope_cache(p, sl.scope);
+    const bool mine = lane < 8 && sl.g >= 0 && (int64_t)sl.g < cd.num_pages * cd.P &&
+                      in_range(((int64_t)sl.g + 1) * kBf16RowBytes <= cd.num_pages * cd.P * kBf16RowBytes, p.status);
+    ok = __ballot_sync(0xffffffffu, mine) & 0xFFu;
+    // pages hold P rows of 1024 bytes back to back, so slot g sits at byte 1024 g
+    const uint64_t rp = reinterpret_cast<uint64_t>(cd.base) + (mine ? (uint64_t)sl.g * kBf16RowBytes : 0u);
+#pragma unroll
+    for (int st = 0; st < 16; ++st) {
+      const int ri = (st + q) & 7;
+      const uint64_t r = __shfl_sync(0xffffffffu, rp, ri);
+      v[st] = make_uint4(0, 0, 0, 0);
+      if ((ok >> ri) & 1u) v[st] = ldg_nc_v4(reinterpret_cast<const uint8_t*>(r) + st * 64 + mm * 16);
+    }
+  };
+  TileCursor c;
+  c.init(p, cid);
+  bool v0 = c.valid(p);
+  SlotRef s0 = slot(c, v0);
+  if (v0) c.next(p);
+  bool v1 = c.valid(p);
+  SlotRef s1 = slot(c, v1);
+  if (v1) c.next(p);
+  load(s0);
+  for (int j = 0; v0; ++j) {
+    const int st_ = j & 1;
+    if (j >= kStages && !wait_warp(&m->kempty[st_], ((j >> 1) - 1) & 1, m, limit)) {
+      if (lane == 0) record_abort(m, p.status);
+      return;
+    }
+    uint8_t* stage = smem + kOffStage + st_ * kStageBytes;
+#pragma unroll
+    for (int st = 0; st < 16; ++st) {
+      const uint32_t ri = (st + q) & 7;
+      *reinterpret_cast<uint4*>(stage + (st >> 1) * kSlab + (8 * cw + ri) * 128 + (((4 * (st & 1) + mm) ^ ri) << 4)) =
+          scrub_bf16x8(v[st]);
+    }
+    if (lane < 8) m->valid[st_][8 * cw + lane] = (ok >> lane) & 1u;
+    fence_async_smem();
+    warp_arrive(&m->kfull[st_]);
+    v0 = v1;
+    s0 = s1;
+    v1 = c.valid(p);
+    s1 = slot(c, v1);
+    if (v1) c.next(p);
+    if (v0) load(s0);
+  }
+}
+
 // ------------------------------------------------------------------ softmax + epilogue
 __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int cid, uint32_t tmem, int warp,
                               int lane) {
@@ -479,7 +577,7 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
     const float sink_nat = (p.S == 1 && p.sink != nullptr && head_ok) ? __ldg(p.sink + h) : -INFINITY;
     const int64_t orow = p.S == 1 ? (int64_t)it.t * p.H + h : ((int64_t)it.t * p.S + it.split) * p.H + h;
     if (it.n == 0) {  // no entries: out = 0 and lse = sink (one split), or an empty split
-      if (head_ok && half == 0) {
+      if (head_ok && half == 0 && in_range(orow < (int64_t)p.T * p.S * p.H, p.status)) {
         if (p.S > 1) p.lse_part[orow] = -INFINITY;
         else if (p.lse != nullptr) p.lse[orow] = sink_nat;
       }
@@ -487,9 +585,11 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
         const int d = 32 * warp + lane;
         for (int hh = 0; hh < kHeads && it.g * kHeads + hh < p.H; ++hh)
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            reinterpret_cast<__nv_bfloat16*>(p.out)[((int64_t)it.t * p.H + it.g * kHeads + hh) * kLatent + 128 * c + d] =
-                __float2bfloat16_rn(0.f);
+          for (int c = 0; c < 4; ++c) {
+            const int64_t off = ((int64_t)it.t * p.H + it.g * kHeads + hh) * kLatent + 128 * c + d;
+            if (in_range(off < (int64_t)p.T * p.H * kLatent, p.status))
+              reinterpret_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(0.f);
+          }
       }
       continue;
     }
@@ -594,7 +694,7 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
     const int fb = nitem & 1;
     if (half == 0) {
       m->factor[fb][n] = factor;
-      if (head_ok) {
+      if (head_ok && in_range(orow < (int64_t)p.T * p.S * p.H, p.status)) {
         if (p.S > 1) p.lse_part[orow] = lse_v;
         else if (p.lse != nullptr) p.lse[orow] = lse_v;
       }
@@ -629,8 +729,8 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
         const int hr = 4 * k + (lane >> 3), dd = 4 * (lane & 7);  // head row, first of 4 dims
         const float4 v = *reinterpret_cast<const float4*>(stg + hr * 32 + dd);
         const float f = m->factor[fb][h0 + hr];
-        if (h0 + hr < hvalid) {
-          const int64_t off = (row_base + h0 + hr) * kLatent + blk * 128 + 32 * warp + dd;
+        const int64_t off = (row_base + h0 + hr) * kLatent + blk * 128 + 32 * warp + dd;
+        if (h0 + hr < hvalid && in_range(off + 4 <= (int64_t)p.T * p.S * p.H * kLatent, p.status)) {
           if (p.S == 1) {
             *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off) =
                 make_uint2(bf16x2_bits(__floats2bfloat162_rn(v.x * f, v.y * f)),
@@ -656,7 +756,7 @@ struct KernelParams {
   CUtensorMap qmap;  // the type carries the 64-byte alignment of a tensor map
 };
 
-template <bool ALIGN16>
+template <bool ALIGN16, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ KernelParams kp) {
   const AttnParams& p = kp.p;
   extern __shared__ uint8_t smem_raw[];
@@ -670,7 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&m->kfull[s], kConvWarps / 2);  // the four warps of the stage's converter group
+      // fp8 rows: the four warps of the stage's converter group; bf16 rows: all eight
+      mbar_init(&m->kfull[s], FMT == 0 ? kConvWarps / 2 : kConvWarps);
       mbar_init(&m->kempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -709,7 +810,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     else if (warp == kPvWarp) pv_warp(smem, m, p, cid, tmem, lane);
   } else {
     regs_inc<kConvRegs>();
-    converter_warps<ALIGN16>(smem, m, p, cid, warp - kConvWarp0, lane);
+    if constexpr (FMT == 0)
+      converter_warps<ALIGN16>(smem, m, p, cid, warp - kConvWarp0, lane);
+    else
+      converter_warps_bf16(smem, m, p, cid, warp - kConvWarp0, lane);
   }
 
   // TMEM is freed only after every tcgen05 access of this CTA is done.
@@ -759,30 +863,26 @@ bool make_q_map(const AttnParams& p, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool A16>
+template <bool A16, int FMT>
 cudaError_t set_smem_attr() {
-  // once per process and device; a racing first call on two threads sets the same value
+  // once per thread and device (the attribute is per function and device; setting it again
+  // with the same value from another thread is harmless)
   static thread_local bool done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(attn_kernel<A16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLaunch);
+  e = cudaFuncSetAttribute(attn_kernel<A16, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLaunch);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
-}  // namespace
 
-cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
-  if (p.T == 0) return cudaSuccess;
-  KernelParams kp;
-  kp.p = p;
-  if (!make_q_map(p, &kp.qmap)) return cudaErrorInvalidValue;
-  const bool a16 = ((int64_t)p.P * kRowBytes) % 16 == 0;
-  cudaError_t e = a16 ? set_smem_attr<true>() : set_smem_attr<false>();
+template <bool A16, int FMT>
+cudaError_t launch_variant(const KernelParams& kp, cudaStream_t s) {
+  cudaError_t e = set_smem_attr<A16, FMT>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.G, 1, 1);
+  cfg.gridDim = dim3(kp.p.G, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemLaunch;
   cfg.stream = s;
@@ -791,7 +891,19 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return a16 ? cudaLaunchKernelEx(&cfg, attn_kernel<true>, kp) : cudaLaunchKernelEx(&cfg, attn_kernel<false>, kp);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<A16, FMT>, kp);
+}
+}  // namespace
+
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  KernelParams kp;
+  kp.p = p;
+  if (!make_q_map(p, &kp.qmap)) return cudaErrorInvalidValue;
+  if (p.fmt == 1) return launch_variant<true, 1>(kp, s);
+  // fp8 data rows are 16-byte aligned when both caches' pages hold an even number of slots
+  const bool a16 = ((int64_t)p.cache.P * kRowBytes) % 16 == 0 && ((int64_t)p.cache2.P * kRowBytes) % 16 == 0;
+  return a16 ? launch_variant<true, 0>(kp, s) : launch_variant<false, 0>(kp, s);
 }
 
 }  // namespace smd

@@ -10,6 +10,8 @@
 // 16 bytes wide and a warp's output row is one contiguous 1 KB write.  The NoPE pieces go
 // through dequant_piece and the RoPE pieces through scrub_bf16x8, the same routines the
 // attention kernel's converters run, so this export pins the hot path's dequantisation.
+// A bf16 cache (1024-byte rows) is copied with scrub_bf16x8 on every piece, as the
+// attention kernel's bf16 converters do.
 #include "smd_device.cuh"
 #include "smd_internal.h"
 
@@ -22,7 +24,13 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherParams p) {
   if (row >= p.rows) return;
   const int32_t slot = __ldg(p.gidx + row);
   uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-  if (slot >= 0 && (int64_t)slot < p.num_pages * p.P) {
+  if (p.fmt == 1) {
+    if (slot >= 0 && (int64_t)slot < p.num_pages * p.P) {
+      const uint8_t* src = p.cache + (int64_t)slot * (kLatent * 2) + lane * 32;
+      lo = scrub_bf16x8(ldg16<true>(src));
+      hi = scrub_bf16x8(ldg16<true>(src + 16));
+    }
+  } else if (slot >= 0 && (int64_t)slot < p.num_pages * p.P) {
     const CacheView c = make_cache_view(p.cache, p.P);
     const uint8_t* data = row_data(c, slot);
     if (lane < 28) {
@@ -41,7 +49,7 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherParams p) {
 cudaError_t launch_gather_dequant(const GatherParams& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((p.rows + 7) / 8);
-  if (((int64_t)p.P * kRowBytes) % 16 == 0)
+  if (p.fmt == 1 || ((int64_t)p.P * kRowBytes) % 16 == 0)
     gather_dequant_kernel<true><<<blocks, 256, 0, s>>>(p);
   else
     gather_dequant_kernel<false><<<blocks, 256, 0, s>>>(p);

@@ -62,8 +62,40 @@ int check_dims(const smd_dims* d) {
     return fail(SMD_ERR_INVALID_ARG, "topk_stride %lld < topk", (long long)d->topk_stride);
   if (d->swa > 0 && d->swa_stride < d->swa)
     return fail(SMD_ERR_INVALID_ARG, "swa_stride %lld < swa", (long long)d->swa_stride);
+  if (d->cache_format != SMD_CACHE_FP8_DS_MLA && d->cache_format != SMD_CACHE_BF16)
+    return fail(SMD_ERR_INVALID_ARG, "cache_format %d is neither 0 (fp8_ds_mla) nor 1 (bf16)", d->cache_format);
   return SMD_OK;
 }
+
+bool has_swa_cache(const smd_decode_opts* o) { return o != nullptr && o->swa_kv_cache != nullptr; }
+
+// What each entry point reads of the window scope's options: the decode both the cache and
+// its block table, the conversion only the block table, the attention only the cache.
+enum class OptsUse { kDecode, kConvert, kAttention };
+
+int check_opts(const smd_decode_opts* o, OptsUse use) {
+  if (o == nullptr) return SMD_OK;
+  const bool cache = o->swa_kv_cache != nullptr, table = o->swa_block_table != nullptr;
+  if (use == OptsUse::kDecode && cache != table)
+    return fail(SMD_ERR_INVALID_ARG, "swa_kv_cache and swa_block_table must be given together");
+  const bool paged = (cache && use != OptsUse::kConvert) || (table && use != OptsUse::kAttention);
+  if (!paged) return SMD_OK;
+  if (o->swa_block_size < 1) return fail(SMD_ERR_INVALID_ARG, "swa_block_size %d < 1", o->swa_block_size);
+  if (o->swa_num_pages < 1) return fail(SMD_ERR_INVALID_ARG, "swa_num_pages %lld < 1", (long long)o->swa_num_pages);
+  if (o->swa_num_pages > (int64_t)INT32_MAX / o->swa_block_size)
+    return fail(SMD_ERR_INVALID_ARG, "swa_num_pages * swa_block_size must stay below 2^31");
+  if (cache && use != OptsUse::kConvert && !aligned16(o->swa_kv_cache))
+    return fail(SMD_ERR_INVALID_ARG, "swa_kv_cache not 16-byte aligned");
+  if (table && use != OptsUse::kAttention) {
+    if (o->swa_max_blocks_per_req < 1)
+      return fail(SMD_ERR_INVALID_ARG, "swa_max_blocks_per_req %d < 1", o->swa_max_blocks_per_req);
+    if (o->swa_bt_stride < o->swa_max_blocks_per_req)
+      return fail(SMD_ERR_INVALID_ARG, "swa_bt_stride %lld < swa_max_blocks_per_req", (long long)o->swa_bt_stride);
+  }
+  return SMD_OK;
+}
+
+bool compacting(const smd_decode_opts* o) { return o != nullptr && o->compact != 0; }
 
 int device_sms(int num_sms) {
   if (num_sms > 0) return num_sms;
@@ -102,7 +134,7 @@ int select_splits(const smd_dims* d, int request, int sms) {
 }
 
 struct Layout {
-  size_t status = 0, gidx = 0, o_part = 0, lse_part = 0, total = 0;
+  size_t status = 0, gidx = 0, counts = 0, o_part = 0, lse_part = 0, total = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -115,6 +147,8 @@ Layout workspace_layout(const smd_dims* d, int S) {
   off += 256;
   L.gidx = off;
   off += up256(T * N * sizeof(int32_t));
+  L.counts = off;
+  off += up256(T * 2 * sizeof(int32_t));
   if (S > 1) {
     L.o_part = off;
     off += up256(T * (size_t)S * H * SMD_LATENT_DIM * sizeof(float));
@@ -126,15 +160,17 @@ Layout workspace_layout(const smd_dims* d, int S) {
 }
 
 // Attention launch parameters shared by the whole-step and the stage entry points.
-smd::AttnParams attn_params(const smd_dims* d, int S, int sms, const void* q, const uint8_t* cache,
-                            const int32_t* gidx, const float* sink, float scale, void* out, float* lse,
-                            float* o_part, float* lse_part, uint32_t* status) {
+smd::AttnParams attn_params(const smd_dims* d, const smd_decode_opts* o, int S, int sms, const void* q,
+                            const uint8_t* cache, const int32_t* gidx, const int32_t* counts, const float* sink,
+                            float scale, void* out, float* lse, float* o_part, float* lse_part, uint32_t* status) {
   const int64_t N = (int64_t)d->topk + d->swa;
   const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
   smd::AttnParams a{};
   a.q = q;
-  a.cache = cache;
+  a.cache = smd::CacheDesc{cache, d->num_pages, d->block_size};
+  a.cache2 = has_swa_cache(o) ? smd::CacheDesc{o->swa_kv_cache, o->swa_num_pages, o->swa_block_size} : a.cache;
   a.gidx = gidx;
+  a.counts = counts;
   a.sink = sink;
   a.out = out;
   a.lse = lse;
@@ -142,12 +178,12 @@ smd::AttnParams attn_params(const smd_dims* d, int S, int sms, const void* q, co
   a.lse_part = S > 1 ? lse_part : nullptr;
   a.status = status;
   a.scale = scale;
-  a.num_pages = d->num_pages;
   a.T = d->num_tokens;
   a.H = d->num_heads;
   a.N = (int32_t)N;
-  a.P = d->block_size;
+  a.K = d->topk;
   a.S = S;
+  a.fmt = d->cache_format;
   a.tiles_per_split = (int32_t)((tiles + S - 1) / S);
   if (a.tiles_per_split < 1) a.tiles_per_split = 1;
   a.HG = smd::attn_ctas_per_split(d->num_heads);
@@ -156,8 +192,9 @@ smd::AttnParams attn_params(const smd_dims* d, int S, int sms, const void* q, co
   return a;
 }
 
-smd::ConvertParams convert_params(const smd_dims* d, const int32_t* bt, const int32_t* req,
-                                  const int32_t* topk, const int32_t* swa, int32_t* gidx, uint32_t* status) {
+smd::ConvertParams convert_params(const smd_dims* d, const smd_decode_opts* o, const int32_t* bt,
+                                  const int32_t* req, const int32_t* topk, const int32_t* swa, int32_t* gidx,
+                                  int32_t* counts, uint32_t* status) {
   smd::ConvertParams p{};
   p.block_table = bt;
   p.req_id = req;
@@ -165,6 +202,18 @@ smd::ConvertParams convert_params(const smd_dims* d, const int32_t* bt, const in
   p.swa = swa;
   p.gidx = gidx;
   p.status = status;
+  if (o != nullptr) {
+    p.topk_length = o->topk_length;
+    if (o->swa_block_table != nullptr) {
+      p.swa_block_table = o->swa_block_table;
+      p.swa_max_blocks = o->swa_max_blocks_per_req;
+      p.swa_P = o->swa_block_size;
+      p.swa_num_pages = o->swa_num_pages;
+      p.swa_bt_stride = o->swa_bt_stride;
+    }
+    p.compact = o->compact != 0;
+  }
+  p.counts = p.compact ? counts : nullptr;
   p.T = d->num_tokens;
   p.R = d->num_requests;
   p.max_blocks = d->max_blocks_per_req;
@@ -205,7 +254,7 @@ extern "C" {
 
 SMD_API const char* smd_last_error(void) { return g_err; }
 
-SMD_API int smd_version(void) { return 100; }
+SMD_API int smd_version(void) { return 200; }
 
 SMD_API int smd_select_num_splits(const smd_dims* dims, int num_splits, int num_sms) {
   g_err[0] = '\0';
@@ -237,9 +286,61 @@ SMD_API int smd_convert_req_index(const smd_dims* dims, const int32_t* block_tab
   if (rc != SMD_OK) return rc;
   if (dims->num_tokens > 0 && dims->topk + dims->swa > 0 && gidx == nullptr)
     return fail(SMD_ERR_INVALID_ARG, "gidx is NULL");
-  const cudaError_t e =
-      smd::launch_convert(convert_params(dims, block_table, req_id, topk_idx, swa_idx, gidx, nullptr), stream);
+  const cudaError_t e = smd::launch_convert(
+      convert_params(dims, nullptr, block_table, req_id, topk_idx, swa_idx, gidx, nullptr, nullptr), stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "convert launch");
+}
+
+SMD_API int smd_convert_req_index_ex(const smd_dims* dims, const smd_decode_opts* opts, const int32_t* block_table,
+                                     const int32_t* req_id, const int32_t* topk_idx, const int32_t* swa_idx,
+                                     int32_t* gidx, int32_t* counts, smd_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  rc = check_opts(opts, OptsUse::kConvert);
+  if (rc != SMD_OK) return rc;
+  rc = check_index_ptrs(dims, block_table, req_id, topk_idx, swa_idx);
+  if (rc != SMD_OK) return rc;
+  if (dims->num_tokens > 0 && dims->topk + dims->swa > 0 && gidx == nullptr)
+    return fail(SMD_ERR_INVALID_ARG, "gidx is NULL");
+  if (dims->num_tokens > 0 && compacting(opts) && counts == nullptr)
+    return fail(SMD_ERR_INVALID_ARG, "counts is required with compact");
+  const cudaError_t e = smd::launch_convert(
+      convert_params(dims, opts, block_table, req_id, topk_idx, swa_idx, gidx, counts, nullptr), stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "convert launch");
+}
+
+SMD_API int smd_convert_req_index_ragged(const smd_dims* dims, const int32_t* block_table, const int32_t* req_id,
+                                         const int32_t* token_indices, int32_t num_cols, int64_t ti_stride,
+                                         const int32_t* cu_seqlens, int32_t* out, smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (dims == nullptr) return fail(SMD_ERR_INVALID_ARG, "dims is NULL");
+  if (dims->num_tokens < 0 || dims->num_tokens > kMaxTokens)
+    return fail(SMD_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", dims->num_tokens, kMaxTokens);
+  if (dims->num_requests < 1 || dims->max_blocks_per_req < 1 || dims->block_size < 1 ||
+      dims->bt_stride < dims->max_blocks_per_req)
+    return fail(SMD_ERR_INVALID_ARG, "bad num_requests/max_blocks_per_req/block_size/bt_stride");
+  if (num_cols < 0 || ti_stride < num_cols)
+    return fail(SMD_ERR_INVALID_ARG, "num_cols %d < 0 or ti_stride %lld < num_cols", num_cols, (long long)ti_stride);
+  if (dims->num_tokens == 0) return SMD_OK;
+  if (block_table == nullptr || req_id == nullptr || cu_seqlens == nullptr || out == nullptr ||
+      (num_cols > 0 && token_indices == nullptr))
+    return fail(SMD_ERR_INVALID_ARG, "block_table, req_id, token_indices, cu_seqlens and out are required");
+  smd::RaggedParams p{};
+  p.req_id = req_id;
+  p.block_table = block_table;
+  p.token_indices = token_indices;
+  p.cu_seqlens = cu_seqlens;
+  p.out = out;
+  p.T = dims->num_tokens;
+  p.R = dims->num_requests;
+  p.max_blocks = dims->max_blocks_per_req;
+  p.P = dims->block_size;
+  p.num_cols = num_cols;
+  p.bt_stride = dims->bt_stride;
+  p.ti_stride = ti_stride;
+  const cudaError_t e = smd::launch_convert_ragged(p, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "ragged convert launch");
 }
 
 SMD_API int smd_gather_dequant(const smd_dims* dims, const uint8_t* kv_cache, const int32_t* gidx,
@@ -253,7 +354,9 @@ SMD_API int smd_gather_dequant(const smd_dims* dims, const uint8_t* kv_cache, co
   if (kv_cache == nullptr || gidx == nullptr || kv_out == nullptr)
     return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned16(kv_cache) || !aligned16(kv_out)) return fail(SMD_ERR_INVALID_ARG, "kv_cache/kv_out not 16-byte aligned");
-  smd::GatherParams p{kv_cache, gidx, kv_out, num_rows, dims->num_pages, dims->block_size};
+  if (dims->cache_format != SMD_CACHE_FP8_DS_MLA && dims->cache_format != SMD_CACHE_BF16)
+    return fail(SMD_ERR_INVALID_ARG, "cache_format %d is neither 0 nor 1", dims->cache_format);
+  smd::GatherParams p{kv_cache, gidx, kv_out, num_rows, dims->num_pages, dims->block_size, dims->cache_format};
   const cudaError_t e = smd::launch_gather_dequant(p, stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "gather launch");
 }
@@ -273,12 +376,15 @@ SMD_API int smd_lse_combine(int32_t num_tokens, int32_t num_splits, int32_t num_
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "combine launch");
 }
 
-SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
-                                  const int32_t* block_table, const int32_t* req_id, const int32_t* topk_idx,
-                                  const int32_t* swa_idx, const float* sink, float scale, void* out, float* lse,
-                                  int num_splits, void* workspace, size_t workspace_bytes, smd_stream_t stream) {
+SMD_API int smd_sparse_mla_decode_ex(const smd_dims* dims, const smd_decode_opts* opts, const void* q,
+                                     const uint8_t* kv_cache, const int32_t* block_table, const int32_t* req_id,
+                                     const int32_t* topk_idx, const int32_t* swa_idx, const float* sink, float scale,
+                                     void* out, float* lse, int num_splits, void* workspace, size_t workspace_bytes,
+                                     smd_stream_t stream) {
   g_err[0] = '\0';
   int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  rc = check_opts(opts, OptsUse::kDecode);
   if (rc != SMD_OK) return rc;
   rc = check_index_ptrs(dims, block_table, req_id, topk_idx, swa_idx);
   if (rc != SMD_OK) return rc;
@@ -300,15 +406,16 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   int32_t* gidx = reinterpret_cast<int32_t*>(ws + L.gidx);
+  int32_t* counts = compacting(opts) ? reinterpret_cast<int32_t*>(ws + L.counts) : nullptr;
 
   cudaError_t e = smd::launch_convert(
-      convert_params(dims, block_table, req_id, topk_idx, swa_idx, gidx, status), stream);
+      convert_params(dims, opts, block_table, req_id, topk_idx, swa_idx, gidx, counts, status), stream);
   if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   if (dims->num_tokens == 0) return SMD_OK;
 
   const smd::AttnParams a =
-      attn_params(dims, S, sms, q, kv_cache, gidx, sink, scale, out, lse, reinterpret_cast<float*>(ws + L.o_part),
-                  reinterpret_cast<float*>(ws + L.lse_part), status);
+      attn_params(dims, opts, S, sms, q, kv_cache, gidx, counts, sink, scale, out, lse,
+                  reinterpret_cast<float*>(ws + L.o_part), reinterpret_cast<float*>(ws + L.lse_part), status);
   e = smd::launch_attn(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (S > 1) {
@@ -319,12 +426,22 @@ SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uin
   return SMD_OK;
 }
 
-SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
-                                     const int32_t* gidx, const float* sink, float scale, int num_splits,
-                                     void* out, float* lse, float* o_part, float* lse_part, int32_t* status,
-                                     smd_stream_t stream) {
+SMD_API int smd_sparse_mla_decode(const smd_dims* dims, const void* q, const uint8_t* kv_cache,
+                                  const int32_t* block_table, const int32_t* req_id, const int32_t* topk_idx,
+                                  const int32_t* swa_idx, const float* sink, float scale, void* out, float* lse,
+                                  int num_splits, void* workspace, size_t workspace_bytes, smd_stream_t stream) {
+  return smd_sparse_mla_decode_ex(dims, nullptr, q, kv_cache, block_table, req_id, topk_idx, swa_idx, sink, scale,
+                                  out, lse, num_splits, workspace, workspace_bytes, stream);
+}
+
+SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const smd_decode_opts* opts, const void* q,
+                                     const uint8_t* kv_cache, const int32_t* gidx, const int32_t* counts,
+                                     const float* sink, float scale, int num_splits, void* out, float* lse,
+                                     float* o_part, float* lse_part, int32_t* status, smd_stream_t stream) {
   g_err[0] = '\0';
-  const int rc = check_dims(dims);
+  int rc = check_dims(dims);
+  if (rc != SMD_OK) return rc;
+  rc = check_opts(opts, OptsUse::kAttention);
   if (rc != SMD_OK) return rc;
   if (num_splits < -SMD_MAX_SPLITS) return fail(SMD_ERR_INVALID_ARG, "num_splits %d < -%d", num_splits, SMD_MAX_SPLITS);
   if (dims->num_tokens == 0) return SMD_OK;
@@ -340,8 +457,8 @@ SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const void* q, const 
   if (!aligned16(q) || !aligned16(kv_cache) || (out != nullptr && !aligned16(out)) ||
       (o_part != nullptr && !aligned16(o_part)))
     return fail(SMD_ERR_INVALID_ARG, "q/kv_cache/out/o_part not 16-byte aligned");
-  const smd::AttnParams a = attn_params(dims, S, sms, q, kv_cache, gidx, sink, scale, out, lse, o_part, lse_part,
-                                        reinterpret_cast<uint32_t*>(status));
+  const smd::AttnParams a = attn_params(dims, opts, S, sms, q, kv_cache, gidx, counts, sink, scale, out, lse, o_part,
+                                        lse_part, reinterpret_cast<uint32_t*>(status));
   const cudaError_t e = smd::launch_attn(a, stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "attention launch");
 }
@@ -354,6 +471,7 @@ SMD_API int smd_read_status(const void* workspace, int32_t* device_status, smd_s
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   *device_status = v;
+  if (v & 2) return fail(SMD_ERR_DEVICE_CHECK, "a device range check failed (status 0x%x)", v);
   return v != 0 ? fail(SMD_ERR_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", v) : SMD_OK;
 }
 

@@ -150,6 +150,24 @@ __device__ __forceinline__ void dequant_piece(uint4 in, uint32_t code, uint4& lo
   hi = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
+// ---------------------------------------------------------------- debug range checks
+// Status-word bits: a bounded wait gave up (bit 0), a range check of the SMD_DEBUG build
+// failed (bit 1).
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusDeviceCheck = 2u;
+// In a build with SMD_DEBUG defined, in_range(cond, status) records a failed check in the
+// status word (bit 1) and returns false, so that the caller skips the access; otherwise it
+// is `true` and costs nothing.  The checks restate each address's bounds from the buffer
+// sizes, independently of the masking that already keeps accesses in range.
+#ifdef SMD_DEBUG
+__device__ __forceinline__ bool in_range(bool cond, uint32_t* status) {
+  if (!cond && status != nullptr) atomicOr(status, kStatusDeviceCheck);
+  return cond;
+}
+#else
+__device__ __forceinline__ constexpr bool in_range(bool, uint32_t*) { return true; }
+#endif
+
 // ---------------------------------------------------------------- global loads
 // Loads through the read-only path as volatile PTX: the compiler keeps them in program
 // order and cannot sink them to their first use, so a batch of them is in flight at once.

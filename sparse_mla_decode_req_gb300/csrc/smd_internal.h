@@ -9,17 +9,44 @@ namespace smd {
 constexpr int kTileRows = 64;     // rows per split unit (one attention tile)
 constexpr int kMaxSplits = 32;
 
+// One paged cache of the decode: base, page size and page count (the second one, for the
+// window scope, is optional).
+struct CacheDesc {
+  const uint8_t* base;
+  int64_t num_pages;
+  int32_t P;
+};
+
 struct ConvertParams {
   const int32_t* block_table;
   const int32_t* req_id;
   const int32_t* topk;
   const int32_t* swa;
+  const int32_t* topk_length;  // [T] or null: top-k column k of token t masked when k >= topk_length[t]
+  const int32_t* swa_block_table;  // window scope's own block table, or null (the main one)
   int32_t* gidx;          // [T, K+W]
+  int32_t* counts;        // [T, 2] (valid main entries, valid entries) or null
   uint32_t* status;       // reset to 0 by the launch when non-null
   int32_t T, R, max_blocks, P, K, W;
-  int64_t num_pages, bt_stride, topk_stride, swa_stride;
+  int32_t swa_max_blocks, swa_P;
+  int32_t compact;        // pack each token's valid entries to the front (counts required)
+  int64_t num_pages, bt_stride, topk_stride, swa_stride, swa_num_pages, swa_bt_stride;
 };
 cudaError_t launch_convert(const ConvertParams& p, cudaStream_t s);
+
+// The pages' ragged form: token t fills out[cu[t] .. cu[t+1]) from its first cu[t+1] - cu[t]
+// request-local indices; invalid (negative index or block outside [0, max_blocks)) -> 0.
+struct RaggedParams {
+  const int32_t* req_id;
+  const int32_t* block_table;
+  const int32_t* token_indices;  // [T, ti_stride]
+  const int32_t* cu_seqlens;     // [T + 1]
+  int32_t* out;
+  int32_t T, R, max_blocks, P;
+  int32_t num_cols;              // columns of token_indices; a longer token writes 0 past them
+  int64_t bt_stride, ti_stride;
+};
+cudaError_t launch_convert_ragged(const RaggedParams& p, cudaStream_t s);
 
 struct GatherParams {
   const uint8_t* cache;
@@ -27,6 +54,7 @@ struct GatherParams {
   void* kv_out;           // bf16 [rows, 512]
   int64_t rows, num_pages;
   int32_t P;
+  int32_t fmt;            // 0: fp8_ds_mla rows, 1: bf16 rows
 };
 cudaError_t launch_gather_dequant(const GatherParams& p, cudaStream_t s);
 
@@ -43,8 +71,10 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 struct AttnParams {
   const void* q;          // bf16 [T, H, 512]
-  const uint8_t* cache;
+  CacheDesc cache;        // the main (top-k) scope's cache
+  CacheDesc cache2;       // the window scope's cache (== cache when there is one cache)
   const int32_t* gidx;    // [T, N] converted slots, -1 = masked
+  const int32_t* counts;  // [T, 2] (entries of the main scope, all entries) or null: K and N
   const float* sink;      // [H] or null
   void* out;              // bf16 [T, H, 512]          (S == 1)
   float* lse;             // [T, H] or null            (S == 1)
@@ -52,8 +82,8 @@ struct AttnParams {
   float* lse_part;        // [T, S, H]                 (S > 1)
   uint32_t* status;       // device status word
   float scale;
-  int64_t num_pages;
-  int32_t T, H, N, P, S;
+  int32_t T, H, N, K, S;  // N = row length of gidx; K = entries of the main scope (no counts)
+  int32_t fmt;            // 0: fp8_ds_mla rows, 1: bf16 rows
   int32_t tiles_per_split;
   int32_t HG;             // head groups of 64 (CTAs per token and split)
   int32_t G;              // CTAs launched; CTA c takes work items c, c + G, ...

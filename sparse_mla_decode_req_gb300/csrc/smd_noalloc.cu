@@ -13,7 +13,9 @@
 // library keeps that array until the process exits.  Host code cannot pass g_scratch
 // itself to a kernel (in host code the name is only a host-side stand-in), so the first
 // call on each device looks up its device address with cudaGetSymbolAddress while that
-// device is current and caches it; make that first call before any stream capture.
+// device is current and caches it; make that first call before any stream capture.  The
+// cached address belongs to the device's primary context, so it is stale after
+// cudaDeviceReset.  smd_read_static_scratch_status reads the status word at its start.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -70,4 +72,19 @@ extern "C" SMD_API int smd_sparse_mla_decode_static_scratch(const smd_dims* dims
   // it reads (converted slots, split partials) is written earlier in the same call.
   return smd_sparse_mla_decode(dims, q, kv_cache, block_table, req_id, topk_idx, swa_idx, sink, scale, out, lse,
                                num_splits, scratch, (size_t)SMD_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" SMD_API int smd_read_static_scratch_status(int32_t* device_status, smd_stream_t stream) {
+  if (device_status == nullptr) return smd::set_error(SMD_ERR_INVALID_ARG, "device_status is NULL");
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return smd::set_error(SMD_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (dev >= 0 && dev < kMaxDevices) scratch = g_scratch_ptr[dev];
+  }
+  if (scratch == nullptr)
+    return smd::set_error(SMD_ERR_INVALID_ARG, "no static-scratch decode was made on device %d yet", dev);
+  return smd_read_status(scratch, device_status, stream);
 }

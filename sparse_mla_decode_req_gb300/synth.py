@@ -1,4 +1,5 @@
-"""Seeded synthetic decode workloads in the ``fp8_ds_mla`` paged latent-cache format.
+"""Seeded synthetic decode workloads in the ``fp8_ds_mla`` paged latent-cache format
+(and plain bf16 latent caches).
 
 This module is the one piece shared by the CUDA path's tests/benchmark and by the
 float64 oracle: it makes inputs and nothing else.  It contains none of the decode
@@ -173,6 +174,17 @@ def make_cache(num_pages: int, block_size: int, seed: int, device, chunk_pages: 
         pages[:, : P * ROW_DATA_BYTES] = data.reshape(p1 - p0, P * ROW_DATA_BYTES)
         pages[:, P * ROW_DATA_BYTES:] = scale.reshape(p1 - p0, P * ROW_SCALE_BYTES)
     return cache
+
+
+ROW_BYTES_BF16 = 2 * D_LATENT  # a bf16 cache row: 512 little-endian bf16 values
+
+
+def make_cache_bf16(num_pages: int, block_size: int, seed: int, device) -> torch.Tensor:
+    """A bf16 latent cache u8 [num_pages, P * 1024]: every slot holds 512 N(0,1) values
+    rounded to bf16 (NoPE then RoPE), one row after another."""
+    g = _gen(seed, device)
+    vals = torch.randn(num_pages * block_size, D_LATENT, generator=g, device=device).to(torch.bfloat16)
+    return vals.view(torch.uint8).reshape(num_pages, block_size * ROW_BYTES_BF16)
 
 
 def make_inputs(w: Workload, seed: int | None = None, device="cpu") -> DecodeInputs:

@@ -41,7 +41,7 @@ def test_only_abi_symbols_are_exported(lib):
 
 def _dims(T=4, H=128, K=2048, W=128, P=64, pages=8192, R=4, B=2048):
     return api.Dims(num_tokens=T, num_heads=H, num_requests=R, max_blocks_per_req=B, num_pages=pages,
-                    block_size=P, topk=K, swa=W, pad_=0, bt_stride=B, topk_stride=K, swa_stride=W)
+                    block_size=P, topk=K, swa=W, cache_format=0, bt_stride=B, topk_stride=K, swa_stride=W)
 
 
 def test_split_selector_rules(lib):
@@ -81,15 +81,17 @@ def test_workspace_size_layout(lib):
     d = _dims(T=4, H=128, K=2048, W=128)
     s = api.select_num_splits(d, -8, 152)
     T, N, H = 4, 2176, 128
-    assert api.workspace_size(d, -8, 152) == 256 + up(T * N * 4) + up(T * s * H * 512 * 4) + up(T * s * H * 4)
-    # one split: the status word and the converted slots only
+    assert api.workspace_size(d, -8, 152) == (256 + up(T * N * 4) + up(T * 8) + up(T * s * H * 512 * 4)
+                                              + up(T * s * H * 4))
+    # one split: the status word, the converted slots and the per-token counts only
     d1 = _dims(T=256, H=64, K=512, W=128)
-    assert api.workspace_size(d1, 1, 152) == 256 + up(256 * 640 * 4)
+    assert api.workspace_size(d1, 1, 152) == 256 + up(256 * 640 * 4) + up(256 * 8)
 
 
 @pytest.mark.parametrize("field,value", [("num_heads", 0), ("num_heads", 129), ("block_size", 0),
                                          ("num_pages", 0), ("topk", -1), ("bt_stride", 1),
-                                         ("num_tokens", -1), ("num_tokens", 70000)])
+                                         ("num_tokens", -1), ("num_tokens", 70000), ("cache_format", 2),
+                                         ("cache_format", -1)])
 def test_invalid_dims_rejected_before_any_launch(lib, field, value):
     d = _dims()
     setattr(d, field, value)
@@ -142,12 +144,73 @@ def test_gather_and_attention_host_checks(lib):
     assert rc == api.SMD_ERR_INVALID_ARG and "aligned" in api.last_error()
     assert lib.smd_gather_dequant(ctypes.byref(d), None, None, 0, None, None) == api.SMD_OK
     ad = api.attention_dims(2, 64, 640, 100)
-    rc = lib.smd_sparse_mla_attention(ctypes.byref(ad), al, al, al, None, ctypes.c_float(1.0), -33, al, None,
-                                      None, None, None, None)
+    rc = lib.smd_sparse_mla_attention(ctypes.byref(ad), None, al, al, al, None, None, ctypes.c_float(1.0), -33, al,
+                                      None, None, None, None, None)
     assert rc == api.SMD_ERR_INVALID_ARG and "num_splits" in api.last_error()
     ad0 = api.attention_dims(0, 64, 640, 100)
-    assert lib.smd_sparse_mla_attention(ctypes.byref(ad0), None, None, None, None, ctypes.c_float(1.0), 0, None,
-                                        None, None, None, None, None) == api.SMD_OK
+    assert lib.smd_sparse_mla_attention(ctypes.byref(ad0), None, None, None, None, None, None, ctypes.c_float(1.0),
+                                        0, None, None, None, None, None, None) == api.SMD_OK
+    # a misaligned window cache is refused before any launch
+    o = api.DecodeOpts()
+    o.swa_kv_cache, o.swa_num_pages, o.swa_block_size = base + 8, 10, 64
+    rc = lib.smd_sparse_mla_attention(ctypes.byref(ad), ctypes.byref(o), al, al, al, None, None,
+                                      ctypes.c_float(1.0), 1, al, None, None, None, None, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "swa_kv_cache" in api.last_error()
+
+
+def _opts(**kw):
+    o = api.DecodeOpts()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(swa_kv_cache=4096), "together"),                    # cache without table
+    (dict(swa_block_table=4096), "together"),                 # table without cache
+    (dict(swa_kv_cache=4096, swa_block_table=4096, swa_block_size=0, swa_num_pages=4,
+          swa_max_blocks_per_req=1, swa_bt_stride=1), "swa_block_size"),
+    (dict(swa_kv_cache=4096, swa_block_table=4096, swa_block_size=64, swa_num_pages=0,
+          swa_max_blocks_per_req=1, swa_bt_stride=1), "swa_num_pages"),
+    (dict(swa_kv_cache=4096, swa_block_table=4096, swa_block_size=64, swa_num_pages=1 << 30,
+          swa_max_blocks_per_req=1, swa_bt_stride=1), "2^31"),
+    (dict(swa_kv_cache=4096, swa_block_table=4096, swa_block_size=64, swa_num_pages=4,
+          swa_max_blocks_per_req=8, swa_bt_stride=4), "swa_bt_stride"),
+    (dict(swa_kv_cache=4104, swa_block_table=4096, swa_block_size=64, swa_num_pages=4,
+          swa_max_blocks_per_req=1, swa_bt_stride=1), "aligned"),
+])
+def test_decode_options_rejected_before_any_launch(lib, kw, msg):
+    d = _dims(T=2)
+    ws = ctypes.create_string_buffer(1 << 16)
+    wsp = ctypes.c_void_p((ctypes.addressof(ws) + 255) // 256 * 256)
+    o = _opts(**kw)
+    rc = lib.smd_sparse_mla_decode_ex(ctypes.byref(d), ctypes.byref(o), wsp, wsp, wsp, wsp, wsp, wsp, None,
+                                      ctypes.c_float(1.0), wsp, None, 0, wsp, 1 << 15, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and msg in api.last_error(), api.last_error()
+
+
+def test_convert_ex_and_ragged_host_checks(lib):
+    d = _dims(T=2)
+    p = ctypes.c_void_p(4096)
+    # compaction needs the counts array
+    rc = lib.smd_convert_req_index_ex(ctypes.byref(d), ctypes.byref(_opts(compact=1)), p, p, p, p, p, None, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "counts" in api.last_error()
+    # the conversion reads only the window block table: a table alone is accepted by the
+    # checks (no launch happens here: T = 0)
+    d0 = _dims(T=0)
+    o = _opts(swa_block_table=4096, swa_block_size=32, swa_num_pages=8, swa_max_blocks_per_req=4, swa_bt_stride=4)
+    assert lib.smd_convert_req_index_ex(ctypes.byref(d0), ctypes.byref(o), None, None, None, None, None, None,
+                                        None) == api.SMD_OK
+    # ragged: shape checks, then the empty batch launches nothing
+    rc = lib.smd_convert_req_index_ragged(ctypes.byref(d), p, p, p, 5, 4, p, p, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "ti_stride" in api.last_error()
+    rc = lib.smd_convert_req_index_ragged(ctypes.byref(d), None, p, p, 5, 5, p, p, None)
+    assert rc == api.SMD_ERR_INVALID_ARG and "required" in api.last_error()
+    assert lib.smd_convert_req_index_ragged(ctypes.byref(d0), None, None, None, 0, 0, None, None, None) == api.SMD_OK
+
+
+def test_static_scratch_status_before_any_call(lib):
+    assert lib.smd_read_static_scratch_status(None, None) == api.SMD_ERR_INVALID_ARG
 
 
 def test_version(lib):

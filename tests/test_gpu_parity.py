@@ -260,15 +260,15 @@ def test_decode_all_entries_masked(ns):
     assert torch.all(out2[1:].float() == 0) and torch.all(torch.isneginf(lse2[1:]))
 
 
-@pytest.mark.parametrize("kinds", [(0, 1, 2), (0, 1, 2, 4, 0, 1, 2, 0)])
+@pytest.mark.parametrize("kinds", [(0, 1, 2), (0, 1, 2, 4, 0, 1, 2, 0), (4, 0, 1, 4, 2, 0)])
 def test_decode_poisoned_rows_are_scrubbed(kinds):
     """NaN bytes, NaN scale codes and non-finite RoPE are zeroed before the dot products.
 
-    Kind 4 (one row scaled 2^40 above the rest) dominates its heads' softmax.  It appears
-    once: two such rows would have scores ~2^40 apart from everything else but close to
-    each other, and the two CTAs of a pair exchange their partial scores as int16 fixed
-    point with an absolute error of up to max|partial| * 2^-16, which at that magnitude is
-    far above their gap.
+    Kind 4 (a row whose group-3 scale code is raised to 160, i.e. values about 2^33 times
+    larger) dominates its heads' softmax; the third case has two such rows, whose scores
+    are both of order 2^33 times the rest and far apart from each other, so the larger one
+    takes nearly all the weight on both sides.  Scores are accumulated in fp32 over all
+    512 dims inside one CTA, so their error stays a small relative one.
 
     Kind 3 (code 247: latent values near 2^127) is left to the gather test, where it is
     checked bit for bit: such rows make the fp32 q.k products overflow, a range that fp32
@@ -392,3 +392,39 @@ def test_decode_replays_in_a_cuda_graph(ns):
         assert_out_close(out, ro, f"graph replay splits {ns}")
         assert_lse_close(lse, rl, f"graph replay splits {ns}")
         assert api.read_status(ws) == 0
+
+
+# ----------------------------------------------------------------- bounded waits
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """With the wait bound shortened to 1 ns through the test hook the attention kernel's
+    first wait gives up: the launch records bit 0 in the status word, drains what it has in
+    flight and returns, smd_read_status reports SMD_ERR_TIMEOUT, and the next call with the
+    default bound on the same workspace clears the word and matches the oracle."""
+    w = synth.small_workload(num_tokens=4, num_heads=128, topk=900, swa=100, ctx=3000, n_invalid=20)
+    inp = synth.make_inputs(w, seed=61, device="cuda")
+    dims = api.make_dims(inp.q, inp.kv_cache, inp.block_table, inp.req_id, inp.topk_idx, inp.swa_idx)
+    ws = torch.zeros(api.workspace_size(dims, 1, 0), dtype=torch.uint8, device="cuda")
+
+    def call():
+        return api.sparse_mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.req_id, inp.topk_idx,
+                                     inp.swa_idx, inp.sink, inp.scale, num_splits=1, workspace=ws)
+
+    call()  # per-device set-up before the bound changes
+    torch.cuda.synchronize()
+    prev = api.set_wait_limit_ns(1)
+    try:
+        call()
+        torch.cuda.synchronize()
+    finally:
+        assert api.set_wait_limit_ns(prev) == 1
+    word = int(ws[:4].view(torch.int32).item())
+    assert word & 1, f"status word {word:#x}"
+    with pytest.raises(api.SmdError) as e:
+        api.read_status(ws)
+    assert e.value.status == api.SMD_ERR_TIMEOUT
+    out, lse = call()
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == 0
+    ro, rl = oracle_decode(inp)
+    assert_out_close(out, ro, "after a timed-out launch")
+    assert_lse_close(lse, rl, "after a timed-out launch")

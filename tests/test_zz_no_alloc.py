@@ -16,7 +16,8 @@ import pytest
 import torch
 
 from sparse_mla_decode_req_gb300 import api, build, synth
-from tests.gpu_util import OUT_MAX_ABS, OUT_MEAN_REL, bf16_to_f64
+from tests.gpu_util import (OUT_MAX_ABS, OUT_MEAN_REL, assert_lse_close, assert_out_close, bf16_to_f64,
+                            oracle_decode)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +58,12 @@ def _close(got, ref):
     assert diff.sum() / max(abs(r).sum(), 1e-30) <= OUT_MEAN_REL
 
 
+def _oracle_close(inp, out, lse):
+    ro, rl = oracle_decode(inp)
+    assert_out_close(out, ro, "static scratch")
+    assert_lse_close(lse, rl, "static scratch")
+
+
 def test_static_scratch_matches_regular_entry_point_twice(lib):
     cases = [
         (synth.make_inputs(synth.small_workload(num_tokens=3, num_heads=64, topk=600, swa=100, ctx=2000,
@@ -70,13 +77,35 @@ def test_static_scratch_matches_regular_entry_point_twice(lib):
         _close(out, ref_out)
         assert torch.allclose(lse, ref_lse, rtol=1e-5, atol=1e-3)
         assert torch.isfinite(out.float()).all()
+        _oracle_close(inp, out, lse)
+        assert api.read_static_scratch_status() == 0
+
+
+def test_static_scratch_call_allocates_no_device_memory(lib):
+    """After first calls (which load the library's kernels and its static array), further
+    calls leave the device's free memory exactly as it was (the outputs the helper makes
+    come from torch's caching allocator, which reuses its blocks)."""
+    inp = synth.make_inputs(synth.small_workload(num_tokens=2, num_heads=64, topk=300, swa=60, ctx=900,
+                                                 n_invalid=7), seed=41, device="cuda")
+    inp2 = synth.make_inputs(synth.small_workload(num_tokens=5, num_heads=128, topk=500, swa=0, ctx=1200,
+                                                  n_invalid=3), seed=42, device="cuda")
+    calls = ((inp, -3), (inp2, 1), (inp2, -7))
+    for x, ns in calls:  # also fills torch's caching allocator with the outputs' blocks
+        _static_call(lib, x, ns)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        for x, ns in calls:
+            _static_call(lib, x, ns)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_static_scratch_rejects_oversized_steps(lib):
     # 32 tokens x 32 splits x 128 heads of fp32 partials = 64 MiB > the static array
     w = synth.Workload("too_big", 32, 128, 2048, 0, 4096, 4096)
     d = api.Dims(num_tokens=w.num_tokens, num_heads=w.num_heads, num_requests=w.num_tokens, max_blocks_per_req=64,
-                 num_pages=64 * w.num_tokens, block_size=64, topk=w.topk, swa=0, pad_=0, bt_stride=64,
+                 num_pages=64 * w.num_tokens, block_size=64, topk=w.topk, swa=0, cache_format=0, bt_stride=64,
                  topk_stride=w.topk, swa_stride=0)
     rc = lib.smd_sparse_mla_decode_static_scratch(ctypes.byref(d), None, None, None, None, None, None, None,
                                                   ctypes.c_float(1.0), None, None, -32, None)
