@@ -73,7 +73,9 @@ constexpr uint32_t kPBytes = kSlab;             // P^T [64 heads x 64 rows]
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffStage = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffMisc = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffEpi = kOffP + 2 * kPBytes;    // output staging: 4 KB per softmax warp
+constexpr uint32_t kEpiWarpBytes = 4096;
+constexpr uint32_t kOffMisc = kOffEpi + 4 * kEpiWarpBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
@@ -100,8 +102,8 @@ struct Misc {
   uint32_t abort;
   uint32_t rescale_seq[2];   // tile j + 1 when tile j needs an O^T rescale
   alignas(16) uint8_t valid[kStages][kTile];  // row validity of each stage (read as 16-byte vectors)
-  float alpha[2][kHeads];    // per-head rescale factor of a tile
-  float factor[2][kHeads];   // per-head output factor of an item
+  alignas(16) float alpha[2][kHeads];   // per-head rescale factor of a tile (read as 16-byte vectors)
+  alignas(16) float factor[2][kHeads];  // per-head output factor of an item (read as 16-byte vectors)
 };
 static_assert(offsetof(Misc, valid) % 16 == 0, "valid[] is read with 16-byte loads");
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc);
@@ -325,29 +327,35 @@ __device__ void pv_warp(uint8_t* smem, Misc* m, const AttnParams& p, int cid, ui
 }
 
 // ------------------------------------------------------------------ converters
-// Two groups of four converter warps take alternate tiles (group g: tiles j with j & 1 ==
-// g, always into stage g), so that one group's gathers are in flight while the other
-// converts.  Warp w of a group owns rows 16w .. 16w+15 of its tiles, as two sets of 8 rows
-// moved in 9 steps of one 64-byte segment per row: steps 0-6 the NoPE segments (step st
-// = dims 64st..64st+63, all under scale code st), steps 7-8 the two RoPE halves.  At step
-// st lanes 4i..4i+3 take the segment of row (st + i) mod 8 of the set, so each group of
-// four lanes reads 64 contiguous bytes (whole sectors; a row is fetched by one warp within
-// a few instructions, which keeps DRAM pages open: a layout that spread each row over
-// nine warps gathered at half the rate), and the eight rows of one store instruction hit
-// eight different 16-byte bank groups of the 128B-swizzled stage (row r's chunks are
-// XORed with r & 7).  Lane i < 16 reads row i's slot and 8-byte scale row; the other
-// lanes get them by shuffles.
-constexpr int kConvGroupWarps = kConvWarps / 2;
-constexpr int kRowsPerConvWarp = kTile / kConvGroupWarps;  // 16
-static_assert(kRowsPerConvWarp == 16, "two 8-row sets per converter warp");
+// All eight converter warps take every tile: warp cw owns rows 8cw .. 8cw+7, lanes
+// 4q..4q+3 row 8cw + q, moved in 9 steps of one 64-byte segment (lane m taking bytes
+// 16m .. 16m+15 of it): steps 0-6 the NoPE segments (step st = dims 64st..64st+63, all
+// under scale code st), steps 7-8 the two RoPE halves.  At each step a group of four lanes
+// reads 64 contiguous bytes (whole sectors; a row is fetched by one warp within a few
+// instructions, which keeps DRAM pages open: a layout that spread each row over nine warps
+// gathered at half the rate).  Each lane reads its row's slot and scale row itself.  The
+// eight rows of one store instruction hit eight different 16-byte bank groups of the
+// 128B-swizzled stage (row r's chunks are XORed with r & 7).
+//
+// Every warp keeps two tiles of gathered rows in registers (buffers A and B, for the even
+// and the odd tiles): right after converting a tile into its stage it issues the gathers
+// of the tile two ahead into the same registers, so each warp has one tile of gathers in
+// flight while it converts the other, and a tile's conversion is spread over all warps.
+constexpr int kRowsPerConvWarp = kTile / kConvWarps;  // 8
+static_assert(kRowsPerConvWarp == 8, "one 8-row set per converter warp");
 
 // A row's converted slot and the scope (cache) it lives in.
 struct SlotRef {
   int32_t g;      // -1: masked or past the end
   int32_t scope;  // 0: main cache, 1: window cache
 };
-__device__ __forceinline__ const CacheDesc& scope_cache(const AttnParams& p, int32_t scope) {
-  return scope ? p.cache2 : p.cache;
+__device__ __forceinline__ CacheDesc scope_cache(const AttnParams& p, int32_t scope) {
+  CacheDesc c;
+  c.base = scope ? p.cache2.base : p.cache.base;
+  c.num_pages = scope ? p.cache2.num_pages : p.cache.num_pages;
+  c.P = scope ? p.cache2.P : p.cache.P;
+  c.log2P = scope ? p.cache2.log2P : p.cache.log2P;
+  return c;
 }
 // Issues the read of the slot of entry row `r` of tile `c` (the value is validated where
 // it is used, so the read stays in flight meanwhile).
@@ -362,165 +370,145 @@ __device__ __forceinline__ SlotRef read_slot(const AttnParams& p, const TileCurs
 
 template <bool ALIGN16>
 struct Converter {
-  int lane, q, m;  // q = lane / 4: the row offset of this lane's segments; m = lane % 4: its piece
-  __device__ Converter(int lane_) : lane(lane_), q(lane_ >> 2), m(lane_ & 3) {}
+  int q, m, row;  // q = lane / 4: the lane's row in the warp's 8; m = lane % 4: its piece; row: in the tile
+  __device__ Converter(int lane, int cw) : q(lane >> 2), m(lane & 3), row(kRowsPerConvWarp * cw + (lane >> 2)) {}
   struct Raw {
-    uint4 v[2][9];   // v[h][st]: piece 4st + m of row 8h + ((st + q) & 7) of the warp's 16
-    uint2 sc;        // lane i < 16: scale row of row i
-    uint64_t rptr;   // lane i < 16: address of row i's data
-    uint32_t ok;     // bit i: row i is valid (same in every lane)
+    uint4 v[9];          // v[st]: bytes 64 st + 16 m .. +15 of the lane's row
+    uint2 sc;            // its scale row
+    const uint8_t* rp;   // its data
+    bool ok;             // the row is valid
   };
-  __device__ SlotRef slot(const AttnParams& p, const TileCursor& c, bool v, int w) const {
-    return lane < kRowsPerConvWarp ? read_slot(p, c, v, kRowsPerConvWarp * w + lane) : SlotRef{-1, 0};
-  }
+  __device__ SlotRef slot(const AttnParams& p, const TileCursor& c, bool v) const { return read_slot(p, c, v, row); }
   __device__ void load(const AttnParams& p, SlotRef sl, Raw& d) const {
-    const CacheDesc& cd = scope_cache(p, sl.scope);
-    const bool mine = lane < kRowsPerConvWarp && sl.g >= 0 && (int64_t)sl.g < cd.num_pages * cd.P;
-    d.ok = __ballot_sync(0xffffffffu, mine) & 0xFFFFu;
+    const CacheDesc cd = scope_cache(p, sl.scope);
+    d.ok = false;
     d.sc = make_uint2(0, 0);
-    const uint8_t* row = cd.base;
-    if (mine) {
-      const CacheView cv = make_cache_view(cd.base, cd.P);
+    d.rp = cd.base;
+    if (sl.g >= 0 && (int64_t)sl.g < cd.num_pages * cd.P) {
+      const CacheView cv = make_cache_view(cd.base, cd.P, cd.log2P);
       int32_t page, o;
       slot_page_off(cv, sl.g, page, o);
-      if (!in_range(page >= 0 && page < cd.num_pages && o >= 0 && o < cd.P, p.status)) page = o = 0;
-      const uint8_t* pg = cv.base + (int64_t)page * cv.page_bytes;
-      row = pg + (int64_t)o * kDataBytes;
-      d.sc = ldg_nc_v2(pg + cv.scale_start + (int64_t)o * kScaleBytes);
-    }
-    d.rptr = reinterpret_cast<uint64_t>(row);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int st = 0; st < 9; ++st) {
-        const int ri = 8 * h + ((st + q) & 7);
-        const uint64_t rp = __shfl_sync(0xffffffffu, d.rptr, ri);
-        d.v[h][st] = make_uint4(0, 0, 0, 0);
-        if ((d.ok >> ri) & 1u) d.v[h][st] = ldg16<ALIGN16>(reinterpret_cast<const uint8_t*>(rp) + st * 64 + m * 16);
+      if (in_range(page >= 0 && page < cd.num_pages && o >= 0 && o < cd.P, p.status)) {
+        const uint8_t* pg = cv.base + (int64_t)page * cv.page_bytes;
+        d.rp = pg + (int64_t)o * kDataBytes;
+        d.sc = ldg_nc_v2(pg + cv.scale_start + (int64_t)o * kScaleBytes);
+        d.ok = true;
       }
+    }
+#pragma unroll
+    for (int st = 0; st < 9; ++st) {
+      d.v[st] = make_uint4(0, 0, 0, 0);
+      if (d.ok) d.v[st] = ldg16<ALIGN16>(d.rp + st * 64 + m * 16);
+    }
   }
-  // Straight-line conversion of every piece on the fast path (no NaN byte, code <= 134),
-  // so the unrolled steps interleave and each piece's registers die once it is stored;
+  // Straight-line conversion of every piece on the fast path (no NaN byte, code <= 134);
   // the rare pieces outside that case are read again (an L1/L2 hit) and redone on the
   // exact path afterwards, overwriting their fast result.
-  __device__ void store(const AttnParams& p, uint8_t* stage, int w, const Raw& d) const {
+  __device__ void store(uint8_t* stage, const Raw& d) const {
     uint32_t redo = 0;
+    uint8_t* rrow = stage + row * 128;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t row0 = kRowsPerConvWarp * w + 8 * h;
-#pragma unroll
-      for (int st = 0; st < 7; ++st) {  // NoPE: slab st, chunks 2m and 2m + 1
-        const uint32_t ri = (st + q) & 7;
-        const uint32_t wv = __shfl_sync(0xffffffffu, st < 4 ? d.sc.x : d.sc.y, 8 * h + ri);
-        const uint32_t code = (wv >> (8 * (st & 3))) & 0xFFu;  // code st of the row
-        uint8_t* rb = stage + st * kSlab + (row0 + ri) * 128;
-        uint4 lo, hi;
-        dequant_fast(d.v[h][st], code, lo, hi);
-        redo |= needs_exact(d.v[h][st], code) ? 1u << (7 * h + st) : 0u;
-        *reinterpret_cast<uint4*>(rb + (((2 * m) ^ ri) << 4)) = lo;
-        *reinterpret_cast<uint4*>(rb + (((2 * m + 1) ^ ri) << 4)) = hi;
-      }
-#pragma unroll
-      for (int st = 7; st < 9; ++st) {  // RoPE: slab 7, chunk 4(st - 7) + m
-        const uint32_t ri = (st + q) & 7;
-        *reinterpret_cast<uint4*>(stage + 7 * kSlab + (row0 + ri) * 128 + (((4 * (st - 7) + m) ^ ri) << 4)) =
-            scrub_bf16x8(d.v[h][st]);
-      }
+    for (int st = 0; st < 7; ++st) {  // NoPE: slab st, chunks 2m and 2m + 1
+      const uint32_t code = ((st < 4 ? d.sc.x : d.sc.y) >> (8 * (st & 3))) & 0xFFu;
+      uint8_t* rb = rrow + st * kSlab;
+      uint4 lo, hi;
+      dequant_fast(d.v[st], code, lo, hi);
+      redo |= needs_exact(d.v[st], code) ? 1u << st : 0u;
+      *reinterpret_cast<uint4*>(rb + (((2 * m) ^ q) << 4)) = lo;
+      *reinterpret_cast<uint4*>(rb + (((2 * m + 1) ^ q) << 4)) = hi;
     }
+#pragma unroll
+    for (int st = 7; st < 9; ++st)  // RoPE: slab 7, chunk 4(st - 7) + m
+      *reinterpret_cast<uint4*>(rrow + 7 * kSlab + (((4 * (st - 7) + m) ^ q) << 4)) = scrub_bf16x8(d.v[st]);
     if (__any_sync(0xffffffffu, redo != 0u)) {  // rare: NaN bytes or codes above 134
 #pragma unroll 1
-      for (int i = 0; i < 14; ++i) {
-        const int h = i / 7, st = i - 7 * h;
-        const uint32_t ri = (st + q) & 7;
-        const uint64_t rp = __shfl_sync(0xffffffffu, d.rptr, 8 * h + ri);
-        const uint32_t wv = __shfl_sync(0xffffffffu, st < 4 ? d.sc.x : d.sc.y, 8 * h + ri);
-        if ((redo >> i) & 1u) {
-          const uint4 raw = ldg16<ALIGN16>(reinterpret_cast<const uint8_t*>(rp) + st * 64 + m * 16);
+      for (int st = 0; st < 7; ++st) {
+        if ((redo >> st) & 1u) {
+          const uint4 raw = ldg16<ALIGN16>(d.rp + st * 64 + m * 16);
+          const uint32_t code = ((st < 4 ? d.sc.x : d.sc.y) >> (8 * (st & 3))) & 0xFFu;
           uint4 lo, hi;
-          dequant_piece(raw, (wv >> (8 * (st & 3))) & 0xFFu, lo, hi);
-          uint8_t* rb = stage + st * kSlab + (kRowsPerConvWarp * w + 8 * h + ri) * 128;
-          *reinterpret_cast<uint4*>(rb + (((2 * m) ^ ri) << 4)) = lo;
-          *reinterpret_cast<uint4*>(rb + (((2 * m + 1) ^ ri) << 4)) = hi;
+          dequant_piece(raw, code, lo, hi);
+          uint8_t* rb = rrow + st * kSlab;
+          *reinterpret_cast<uint4*>(rb + (((2 * m) ^ q) << 4)) = lo;
+          *reinterpret_cast<uint4*>(rb + (((2 * m + 1) ^ q) << 4)) = hi;
         }
       }
     }
   }
 };
 
-// Group g's loop: the gathers of its next tile are issued right after a conversion, so
-// they are in flight while the group waits for its stage (the PV of its previous tile)
-// and while the other group converts.
 template <bool ALIGN16>
 __device__ void converter_warps(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int cw, int lane) {
-  const Converter<ALIGN16> cv(lane);
-  const int g = cw / kConvGroupWarps, w = cw % kConvGroupWarps;
+  using Cv = Converter<ALIGN16>;
+  const Cv cv(lane, cw);
   const uint64_t limit = p.wait_limit_ns;
-  uint8_t* stage = smem + kOffStage + g * kStageBytes;
-  typename Converter<ALIGN16>::Raw d;
-  TileCursor c;  // the tile whose slots are read next (this group's tiles only)
+  typename Cv::Raw a, b;  // even and odd tiles
+  TileCursor c;           // the tile whose slot is read next
   c.init(p, cid);
-  auto skip = [&]() {  // the other group's tile
-    if (c.valid(p)) c.next(p);
+  auto take = [&](bool& v, SlotRef& sl) {  // slot of the cursor's tile, then advance
+    v = c.valid(p);
+    sl = cv.slot(p, c, v);
+    if (v) c.next(p);
   };
-  if (g == 1) skip();
-  bool v0 = c.valid(p);
-  SlotRef s0 = cv.slot(p, c, v0, w);
-  skip();
-  skip();
-  bool v1 = c.valid(p);
-  SlotRef s1 = cv.slot(p, c, v1, w);
-  skip();
-  skip();
-  cv.load(p, s0, d);
-  for (int k = 0; v0; ++k) {  // tile j = g + 2k
-    if (k >= 1 && !wait_warp(&m->kempty[g], (k - 1) & 1, m, limit)) {
+  bool va, vb, va2, vb2;
+  SlotRef sa, sb, sa2, sb2;
+  take(va, sa);    // tile 0
+  take(vb, sb);    // tile 1
+  take(va2, sa2);  // tile 2
+  take(vb2, sb2);  // tile 3
+  if (va) cv.load(p, sa, a);
+  if (vb) cv.load(p, sb, b);
+  // One tile into its stage: wait for the stage (PV of the tile two before it), convert,
+  // publish, then gathers of the tile two ahead into the same registers and the slot read
+  // of the tile after that.
+  auto step = [&](typename Cv::Raw& d, int st_, int k, bool& vnext, SlotRef& snext) -> bool {
+    if (k >= 1 && !wait_warp(&m->kempty[st_], (k - 1) & 1, m, limit)) {
       if (lane == 0) record_abort(m, p.status);
-      return;
+      return false;
     }
-    cv.store(p, stage, w, d);
-    if (lane < kRowsPerConvWarp) m->valid[g][kRowsPerConvWarp * w + lane] = (d.ok >> lane) & 1u;
+    cv.store(smem + kOffStage + st_ * kStageBytes, d);
+    if (cv.m == 0) m->valid[st_][cv.row] = d.ok ? 1u : 0u;
     fence_async_smem();
-    warp_arrive(&m->kfull[g]);
-    // this group's next tile: gathers in flight now, slots of the one after
-    v0 = v1;
-    s0 = s1;
-    v1 = c.valid(p);
-    s1 = cv.slot(p, c, v1, w);
-    skip();
-    skip();
-    if (v0) cv.load(p, s0, d);
+    warp_arrive(&m->kfull[st_]);
+    const bool v = vnext;
+    if (v) cv.load(p, snext, d);
+    take(vnext, snext);
+    return v;
+  };
+  for (int k = 0; va; ++k) {  // tiles 2k (buffer a) and 2k + 1 (buffer b)
+    const bool na = step(a, 0, k, va2, sa2);
+    if (!vb) break;
+    const bool nb = step(b, 1, k, vb2, sb2);
+    if (aborted(m)) return;
+    va = na;
+    vb = nb;
   }
 }
 
 // bf16 latent rows (1024 bytes: 512 little-endian bf16, NoPE then RoPE): nothing to
 // dequantise, only the non-finite elements to zero.  All eight converter warps take every
 // tile, warp cw owning rows 8cw .. 8cw+7, moved in 16 steps of one 64-byte segment per
-// row (step st = dims 32st .. 32st+31: slab st/2, chunks 4(st&1) .. +3), lanes 4i..4i+3
-// taking row (st + i) mod 8 as on the fp8 path.  A tile's rows stay in registers while the
-// warp waits for their stage, so the gathers of tile j + 1 are in flight during the
-// wait for the PV of tile j - 1.
+// row (step st = dims 32st .. 32st+31: slab st/2, chunks 4(st&1) .. +3), lanes 4q..4q+3
+// owning row q as on the fp8 path.  A tile's rows stay in registers while the warp waits
+// for their stage, so the gathers of tile j + 1 are in flight during the wait for the PV
+// of tile j - 1.
 constexpr int kBf16RowBytes = 1024;
 __device__ void converter_warps_bf16(uint8_t* smem, Misc* m, const AttnParams& p, int cid, int cw, int lane) {
   const int q = lane >> 2, mm = lane & 3;
   const uint64_t limit = p.wait_limit_ns;
   uint4 v[16];
-  uint32_t ok = 0;
-  auto slot = [&](const TileCursor& c, bool valid) -> SlotRef {
-    return lane < 8 ? read_slot(p, c, valid, 8 * cw + lane) : SlotRef{-1, 0};
-  };
+  bool ok = false;
+  auto slot = [&](const TileCursor& c, bool valid) -> SlotRef { return read_slot(p, c, valid, 8 * cw + q); };
   auto load = [&](SlotRef sl) {
-    const CacheDesc& cd = scope_cache(p, sl.scope);
-    const bool mine = lane < 8 && sl.g >= 0 && (int64_t)sl.g < cd.num_pages * cd.P &&
-                      in_range(((int64_t)sl.g + 1) * kBf16RowBytes <= cd.num_pages * cd.P * kBf16RowBytes, p.status);
-    ok = __ballot_sync(0xffffffffu, mine) & 0xFFu;
+    const CacheDesc cd = scope_cache(p, sl.scope);
+    ok = sl.g >= 0 && (int64_t)sl.g < cd.num_pages * cd.P &&
+         in_range(((int64_t)sl.g + 1) * kBf16RowBytes <= cd.num_pages * cd.P * kBf16RowBytes, p.status);
     // pages hold P rows of 1024 bytes back to back, so slot g sits at byte 1024 g
-    const uint64_t rp = reinterpret_cast<uint64_t>(cd.base) + (mine ? (uint64_t)sl.g * kBf16RowBytes : 0u);
+    const uint8_t* r = cd.base + (ok ? (int64_t)sl.g * kBf16RowBytes : 0);
 #pragma unroll
     for (int st = 0; st < 16; ++st) {
-      const int ri = (st + q) & 7;
-      const uint64_t r = __shfl_sync(0xffffffffu, rp, ri);
       v[st] = make_uint4(0, 0, 0, 0);
-      if ((ok >> ri) & 1u) v[st] = ldg_nc_v4(reinterpret_cast<const uint8_t*>(r) + st * 64 + mm * 16);
+      if (ok) v[st] = ldg_nc_v4(r + st * 64 + mm * 16);
     }
   };
   TileCursor c;
@@ -538,28 +526,25 @@ __device__ void converter_warps_bf16(uint8_t* smem, Misc* m, const AttnParams& p
       if (lane == 0) record_abort(m, p.status);
       return;
     }
-    uint8_t* stage = smem + kOffStage + st_ * kStageBytes;
+    uint8_t* rrow = smem + kOffStage + st_ * kStageBytes + (8 * cw + q) * 128;
 #pragma unroll
-    for (int st = 0; st < 16; ++st) {
-      const uint32_t ri = (st + q) & 7;
-      *reinterpret_cast<uint4*>(stage + (st >> 1) * kSlab + (8 * cw + ri) * 128 + (((4 * (st & 1) + mm) ^ ri) << 4)) =
-          scrub_bf16x8(v[st]);
-    }
-    if (lane < 8) m->valid[st_][8 * cw + lane] = (ok >> lane) & 1u;
+    for (int st = 0; st < 16; ++st)
+      *reinterpret_cast<uint4*>(rrow + (st >> 1) * kSlab + (((4 * (st & 1) + mm) ^ q) << 4)) = scrub_bf16x8(v[st]);
+    if (mm == 0) m->valid[st_][8 * cw + q] = ok ? 1u : 0u;
     fence_async_smem();
     warp_arrive(&m->kfull[st_]);
     v0 = v1;
     s0 = s1;
+    if (v0) load(s0);  // gathers before the next slot reads, as on the fp8 path
     v1 = c.valid(p);
     s1 = slot(c, v1);
     if (v1) c.next(p);
-    if (v0) load(s0);
   }
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-__device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int cid, uint32_t tmem, int warp,
-                              int lane) {
+__device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, const CUtensorMap* omap, int cid,
+                              uint32_t tmem, int warp, int lane) {
   const int n = 16 * warp + (lane & 15);  // head within the group (TMEM lane 32 warp + lane % 16)
   const int half = lane >> 4;             // score columns [32 half, 32 half + 32)
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
@@ -610,13 +595,14 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
       const uint4 va = ld_shared_v4(vaddr), vb = ld_shared_v4(vaddr + 16);
       const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
       float x[32];
-      float tmax = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four chains, not one of 32
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const bool v = ((vw[i >> 2] >> (8 * (i & 3))) & 0xFFu) != 0u;
         x[i] = v ? __uint_as_float(r[i]) * sl2 : -INFINITY;
-        tmax = fmaxf(tmax, x[i]);
+        mx[i & 3] = fmaxf(mx[i & 3], x[i]);
       }
+      float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
       float alpha = 1.f;
       const bool upd = tmax > m_ref + kRescaleThreshold;  // false while everything is masked
@@ -630,12 +616,14 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
       } else {
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = fast_exp2(x[2 * i] - m_ref), p1 = fast_exp2(x[2 * i + 1] - m_ref);
-          psum += p0 + p1;  // the denominator keeps the unrounded weights
+          ps[i & 3] += p0 + p1;  // the denominator keeps the unrounded weights
           pk[i] = bf16x2_bits(__floats2bfloat162_rn(p0, p1));
         }
+        psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
       }
       l_run = l_run * alpha + psum;
       // P^T buffer b was last read by PV of tile j - 2
@@ -660,9 +648,18 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
             uint32_t o[32];
             const uint32_t col = kColO + cc * 32;  // block cc/2, heads 32(cc&1)..+31
             tmem_ld32(tmem + lane_base + col, o);
+            float al[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 a4 = ld_shared_v4(smem_u32(&m->alpha[b][32 * (cc & 1) + 4 * k]));
+              al[4 * k] = __uint_as_float(a4.x);
+              al[4 * k + 1] = __uint_as_float(a4.y);
+              al[4 * k + 2] = __uint_as_float(a4.z);
+              al[4 * k + 3] = __uint_as_float(a4.w);
+            }
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * m->alpha[b][32 * (cc & 1) + i]);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[i]);
             tmem_st32(tmem + lane_base + col, o);
           }
           tmem_wait_st();
@@ -705,47 +702,68 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
     if (!(ok = wait_warp(&m->erdv, nerdv & 1, m, limit))) break;
     ++nerdv;
     tc_fence_after();
-    // O^T (lane = latent dim, column = head) leaves through a warp-private 4 KB slice of
-    // the P^T buffers (free once O is final): per block of 128 dims and 32 heads the warp
-    // writes its 32 dim-lanes of the 32 heads as fp32 rows [head][32 dims], then reads them
-    // back as 16-byte pieces (lanes 8r..8r+7: head row r) and stores 4 consecutive dims of
-    // one head per lane, so a warp store covers whole row segments (64 B of bf16 or 128 B
-    // of fp32 per head) instead of 2 or 4 bytes in each of 32 rows.
-    const int hvalid = min(kHeads, p.H - it.g * kHeads);
-    const int64_t row_base = p.S == 1 ? (int64_t)it.t * p.H + it.g * kHeads
-                                      : ((int64_t)it.t * p.S + it.split) * p.H + it.g * kHeads;
-    float* stg = reinterpret_cast<float*>(smem + kOffP) + warp * 1024;  // [32 heads][32 dims] fp32
+    // O^T (lane = latent dim, column = head) leaves by TMA stores, which take no slot in the
+    // load/store pipeline that the gathers keep busy.  Per block of 128 dims and 32 heads the
+    // warp writes its 32 dim-lanes of the 32 heads, scaled, as the box [32 heads][32 dims]
+    // (bf16 or fp32) into one of its two 4 KB staging buffers (a slice of the P^T buffers,
+    // free once O is final, and a slice of the staging region) and one lane stores the box
+    // to out[t, heads, dims] (or o_part[t, split, heads, dims]); the tensor map clips heads
+    // past H.
+    const int zc = p.S == 1 ? it.t : it.t * p.S + it.split;
+    uint8_t* const buf0 = smem + kOffP + warp * kEpiWarpBytes;
+    uint8_t* const buf1 = smem + kOffEpi + warp * kEpiWarpBytes;
+    const bool odd = lane & 1;
 #pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
       const int blk = cc >> 1, h0 = 32 * (cc & 1);
       uint32_t o[32];
       tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
       tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __uint_as_float(o[i]);
+      if (lane == 0 && cc >= 2) bulk_wait_read<1>();  // the store of block cc - 2 read this buffer
       __syncwarp();
+      uint8_t* sb = (cc & 1) ? buf1 : buf0;
+      // the 32 heads' factors into registers first: loads interleaved with the staging
+      // stores would be kept in order behind them (they may alias) and serialise the block
+      float fac[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int hr = 4 * k + (lane >> 3), dd = 4 * (lane & 7);  // head row, first of 4 dims
-        const float4 v = *reinterpret_cast<const float4*>(stg + hr * 32 + dd);
-        const float f = m->factor[fb][h0 + hr];
-        const int64_t off = (row_base + h0 + hr) * kLatent + blk * 128 + 32 * warp + dd;
-        if (h0 + hr < hvalid && in_range(off + 4 <= (int64_t)p.T * p.S * p.H * kLatent, p.status)) {
-          if (p.S == 1) {
-            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off) =
-                make_uint2(bf16x2_bits(__floats2bfloat162_rn(v.x * f, v.y * f)),
-                           bf16x2_bits(__floats2bfloat162_rn(v.z * f, v.w * f)));
-          } else {
-            *reinterpret_cast<float4*>(p.o_part + off) = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
-          }
-        }
+        const uint4 f4 = ld_shared_v4(smem_u32(&m->factor[fb][h0 + 4 * k]));
+        fac[4 * k] = __uint_as_float(f4.x);
+        fac[4 * k + 1] = __uint_as_float(f4.y);
+        fac[4 * k + 2] = __uint_as_float(f4.z);
+        fac[4 * k + 3] = __uint_as_float(f4.w);
       }
-      __syncwarp();  // the rows are read before the next block overwrites them
+      if (p.S == 1) {
+        // lanes 2k and 2k + 1 (dims 2k, 2k + 1) trade one value per pair of heads (i, i + 1),
+        // so that lane 2k stores head i's bf16 pair and lane 2k + 1 head i + 1's
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float v0 = __uint_as_float(o[i]) * fac[i], v1 = __uint_as_float(o[i + 1]) * fac[i + 1];
+          const float keep = odd ? v1 : v0, give = odd ? v0 : v1;
+          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+          const uint32_t pair = bf16x2_bits(odd ? __floats2bfloat162_rn(got, keep) : __floats2bfloat162_rn(keep, got));
+          *reinterpret_cast<uint32_t*>(sb + (i + (odd ? 1 : 0)) * 64 + (lane & ~1) * 2) = pair;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          *reinterpret_cast<float*>(sb + (i * 32 + lane) * 4) = __uint_as_float(o[i]) * fac[i];
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0 && it.g * kHeads + h0 < p.H) {
+        tma_store_3d(omap, smem_u32(sb), blk * 128 + 32 * warp, it.g * kHeads + h0, zc);
+        bulk_commit();
+      }
     }
+    if (lane == 0) bulk_wait_read<0>();  // the next item writes P^T into the staging
+    __syncwarp();
     tc_fence_before();
     warp_arrive(&m->ofree);  // the next item's first PV may overwrite O^T
   }
   if (!ok) record_abort(m, p.status);
+  if (lane == 0) bulk_wait_all();  // every output store performed before the CTA exits
+  __syncwarp();
 }
 
 }  // namespace
@@ -754,6 +772,7 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, int c
 struct KernelParams {
   AttnParams p;
   CUtensorMap qmap;  // the type carries the 64-byte alignment of a tensor map
+  CUtensorMap omap;  // out [T, H, 512] bf16 (one split) or o_part [T*S, H, 512] fp32, boxes of 32 x 32
 };
 
 template <bool ALIGN16, int FMT>
@@ -770,8 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // fp8 rows: the four warps of the stage's converter group; bf16 rows: all eight
-      mbar_init(&m->kfull[s], FMT == 0 ? kConvWarps / 2 : kConvWarps);
+      // every converter warp fills its rows of every stage
+      mbar_init(&m->kfull[s], kConvWarps);
       mbar_init(&m->kempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -803,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   grid_dep_wait();  // the conversion kernel's slots (and any earlier reader of our outputs)
 
   if (warp < kSoftmaxWarps) {
-    softmax_warps(smem, m, p, cid, tmem, warp, lane);
+    softmax_warps(smem, m, p, &kp.omap, cid, tmem, warp, lane);
   } else if (warp < kConvWarp0) {
     regs_dec<kIssueRegs>();
     if (warp == kQkWarp) qk_warp(smem, m, p, &kp.qmap, cid, tmem, lane);
@@ -863,6 +882,23 @@ bool make_q_map(const AttnParams& p, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The output as [rows of one token (and split)] x [H heads] x [512 dims], stored by boxes of
+// 32 dims x 32 heads from the epilogue's staging (no swizzle).
+bool make_out_map(const AttnParams& p, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const bool one = p.S == 1;
+  const cuuint64_t esize = one ? 2 : 4;
+  const cuuint64_t gdim[3] = {(cuuint64_t)kLatent, (cuuint64_t)p.H, (cuuint64_t)p.T * (one ? 1 : (cuuint64_t)p.S)};
+  const cuuint64_t gstride[2] = {(cuuint64_t)kLatent * esize, (cuuint64_t)p.H * kLatent * esize};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  void* base = one ? p.out : static_cast<void*>(p.o_part);
+  return enc(map, one ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool A16, int FMT>
 cudaError_t set_smem_attr() {
   // once per thread and device (the attribute is per function and device; setting it again
@@ -899,7 +935,7 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
   KernelParams kp;
   kp.p = p;
-  if (!make_q_map(p, &kp.qmap)) return cudaErrorInvalidValue;
+  if (!make_q_map(p, &kp.qmap) || !make_out_map(p, &kp.omap)) return cudaErrorInvalidValue;
   if (p.fmt == 1) return launch_variant<true, 1>(kp, s);
   // fp8 data rows are 16-byte aligned when both caches' pages hold an even number of slots
   const bool a16 = ((int64_t)p.cache.P * kRowBytes) % 16 == 0 && ((int64_t)p.cache2.P * kRowBytes) % 16 == 0;

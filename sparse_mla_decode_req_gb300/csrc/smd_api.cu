@@ -167,8 +167,8 @@ smd::AttnParams attn_params(const smd_dims* d, const smd_decode_opts* o, int S, 
   const int64_t tiles = (N + smd::kTileRows - 1) / smd::kTileRows;
   smd::AttnParams a{};
   a.q = q;
-  a.cache = smd::CacheDesc{cache, d->num_pages, d->block_size};
-  a.cache2 = has_swa_cache(o) ? smd::CacheDesc{o->swa_kv_cache, o->swa_num_pages, o->swa_block_size} : a.cache;
+  a.cache = smd::make_cache_desc(cache, d->num_pages, d->block_size);
+  a.cache2 = has_swa_cache(o) ? smd::make_cache_desc(o->swa_kv_cache, o->swa_num_pages, o->swa_block_size) : a.cache;
   a.gidx = gidx;
   a.counts = counts;
   a.sink = sink;

@@ -40,6 +40,10 @@ __host__ __device__ inline int32_t log2_if_pow2(int32_t P) {
 __device__ __forceinline__ CacheView make_cache_view(const uint8_t* base, int32_t P) {
   return CacheView{base, (int64_t)P * kRowBytes, (int64_t)P * kDataBytes, P, log2_if_pow2(P)};
 }
+// The same with log2(P) already known (-1: not a power of two).
+__device__ __forceinline__ CacheView make_cache_view(const uint8_t* base, int32_t P, int32_t log2P) {
+  return CacheView{base, (int64_t)P * kRowBytes, (int64_t)P * kDataBytes, P, log2P};
+}
 
 // Page and in-page offset of a global slot (shifts for power-of-two page sizes).
 __device__ __forceinline__ void slot_page_off(const CacheView& c, int32_t slot, int32_t& page, int32_t& off) {
@@ -303,6 +307,22 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
                : "memory");
 }
+
+// Store of a 3-D box from shared memory (the tensor map clips it at the tensor's bounds),
+// tracked by the issuing thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups still read their shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until all of this thread's bulk groups are complete (their writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -15,7 +15,18 @@ struct CacheDesc {
   const uint8_t* base;
   int64_t num_pages;
   int32_t P;
+  int32_t log2P;  // log2(P) when P is a power of two, else -1
 };
+// log2(P) for a power of two, else -1.
+inline int32_t log2_if_pow2_host(int32_t P) {
+  if (P <= 0 || (P & (P - 1)) != 0) return -1;
+  int32_t l = 0;
+  while ((1 << l) < P) ++l;
+  return l;
+}
+inline CacheDesc make_cache_desc(const uint8_t* base, int64_t num_pages, int32_t P) {
+  return CacheDesc{base, num_pages, P, log2_if_pow2_host(P)};
+}
 
 struct ConvertParams {
   const int32_t* block_table;
