@@ -101,11 +101,11 @@ struct Misc {
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t rescale_seq[2];   // tile j + 1 when tile j needs an O^T rescale
-  alignas(16) uint8_t valid[kStages][kTile];  // row validity of each stage (read as 16-byte vectors)
+  alignas(16) float mask[kStages][kTile];  // per row of each stage: 0 (valid) or -inf (read as 16-byte vectors)
   alignas(16) float alpha[2][kHeads];   // per-head rescale factor of a tile (read as 16-byte vectors)
   alignas(16) float factor[2][kHeads];  // per-head output factor of an item (read as 16-byte vectors)
 };
-static_assert(offsetof(Misc, valid) % 16 == 0, "valid[] is read with 16-byte loads");
+static_assert(offsetof(Misc, mask) % 16 == 0, "mask[] is read with 16-byte loads");
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc);
 constexpr uint32_t kSmemLaunch = kSmemBytes + 1024;  // slack for aligning the base to 1 KB
 static_assert(kSmemLaunch <= 232448, "shared memory budget");
@@ -467,7 +467,7 @@ __device__ void converter_warps(uint8_t* smem, Misc* m, const AttnParams& p, int
       return false;
     }
     cv.store(smem + kOffStage + st_ * kStageBytes, d);
-    if (cv.m == 0) m->valid[st_][cv.row] = d.ok ? 1u : 0u;
+    if (cv.m == 0) m->mask[st_][cv.row] = d.ok ? 0.f : -INFINITY;
     fence_async_smem();
     warp_arrive(&m->kfull[st_]);
     const bool v = vnext;
@@ -530,7 +530,7 @@ __device__ void converter_warps_bf16(uint8_t* smem, Misc* m, const AttnParams& p
 #pragma unroll
     for (int st = 0; st < 16; ++st)
       *reinterpret_cast<uint4*>(rrow + (st >> 1) * kSlab + (((4 * (st & 1) + mm) ^ q) << 4)) = scrub_bf16x8(v[st]);
-    if (mm == 0) m->valid[st_][8 * cw + q] = ok ? 1u : 0u;
+    if (mm == 0) m->mask[st_][8 * cw + q] = ok ? 0.f : -INFINITY;
     fence_async_smem();
     warp_arrive(&m->kfull[st_]);
     v0 = v1;
@@ -589,17 +589,23 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, const
       tmem_wait_ld();
       tc_fence_before();
       warp_arrive(&m->sfree[b]);  // QK of tile j + 2 may overwrite the buffer
-      // row validity of the tile (published with the stage)
+      // row masks of the tile (published with the stage): 0, or -inf for an invalid row,
+      // whose gathered row is zero so its score is too
       if (!(ok = wait_warp(&m->kfull[b], (j >> 1) & 1, m, limit))) break;
-      const uint32_t vaddr = smem_u32(&m->valid[b][32 * half]);
-      const uint4 va = ld_shared_v4(vaddr), vb = ld_shared_v4(vaddr + 16);
-      const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      float mk[32];
+#pragma unroll
+      for (int k4 = 0; k4 < 8; ++k4) {
+        const uint4 v4 = ld_shared_v4(smem_u32(&m->mask[b][32 * half + 4 * k4]));
+        mk[4 * k4] = __uint_as_float(v4.x);
+        mk[4 * k4 + 1] = __uint_as_float(v4.y);
+        mk[4 * k4 + 2] = __uint_as_float(v4.z);
+        mk[4 * k4 + 3] = __uint_as_float(v4.w);
+      }
       float x[32];
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four chains, not one of 32
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const bool v = ((vw[i >> 2] >> (8 * (i & 3))) & 0xFFu) != 0u;
-        x[i] = v ? __uint_as_float(r[i]) * sl2 : -INFINITY;
+        x[i] = fmaf(__uint_as_float(r[i]), sl2, mk[i]);
         mx[i & 3] = fmaxf(mx[i & 3], x[i]);
       }
       float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));

@@ -97,7 +97,10 @@ __device__ __forceinline__ uint32_t zero_fp8_nans(uint32_t w) {
 // bytes of the two 16-bit halves (0x4140: bytes 0 and 1; 0x4342: bytes 2 and 3).
 __device__ __forceinline__ uint32_t place_fp8x2(uint32_t w, uint32_t sel) {
   const uint32_t y = __byte_perm(w, 0u, sel);  // 0x00bb00aa
-  return ((y << 4) & 0x07F007F0u) | ((y << 8) & 0x80008000u);
+  // y * 16 puts each byte at bits 4..11 of its half, sign at bit 11; adding sign * 240
+  // moves that bit to 15 (+ sign << 8, - sign << 4), with no carry out of a half
+  const uint32_t sgn = y & 0x00800080u;
+  return y * 16u + sgn * 240u;
 }
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
