@@ -757,8 +757,10 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, const
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0 && it.g * kHeads + h0 < p.H) {
-        tma_store_3d(omap, smem_u32(sb), blk * 128 + 32 * warp, it.g * kHeads + h0, zc);
+      if (lane == 0) {
+        // a box wholly past H is not stored, but still closes a (then empty) group, so
+        // that the wait above always counts the store of the other buffer
+        if (it.g * kHeads + h0 < p.H) tma_store_3d(omap, smem_u32(sb), blk * 128 + 32 * warp, it.g * kHeads + h0, zc);
         bulk_commit();
       }
     }

@@ -1,16 +1,5 @@
-// Index conversion: request-local top-k / window positions -> global cache slots.
-//
-// vLLM PR #41217 report, "关键源码片段", _convert_req_index_to_global_index_kernel: for
-// each (token, column) the block is index // P and the in-page offset index % P; the block
-// must lie in [0, max_num_blocks_per_req) and the slot is block_table[req, block] * P +
-// offset.  The physical page is also range-checked against the cache, as the cp-gather
-// kernel of vLLM PR #52212 report ("关键源码片段") does.  Window entries follow the top-k
-// entries at column offset K (SGLang PR #26208 report, _gather_dequant_dsv4_kernel's
-// k_offset); when the window scope has its own cache, its entries go through that cache's
-// block table and page size (vLLM PR #52212 report, "实现拆解" items 1 and 3: main and
-// SWA scopes over the compressed and the window cache).  A top-k column k of token t is
-// masked when k >= TopkLength[t] (SGLang PR #26208 report, "关键源码片段",
-// HAS_TOPK_LENGTH).
+// Index conversion: request-local top-k / window positions -> global cache slots, by the
+// rule of smd_index.cuh.
 //
 // Three kernels:
 //   convert_kernel: dense [T, K+W] output, -1 for invalid entries; one thread per entry,
@@ -30,6 +19,7 @@
 // In an SMD_DEBUG build a failed range check here sets bit 1 of the status word; one made
 // by another CTA before CTA 0 resets the word in the same launch can be lost.
 #include "smd_device.cuh"
+#include "smd_index.cuh"
 #include "smd_internal.h"
 
 namespace smd {
@@ -37,22 +27,9 @@ namespace {
 
 // Slot of column j of token t under the dense rule, -1 if invalid.
 __device__ __forceinline__ int32_t convert_one(const ConvertParams& p, int32_t t, int32_t j) {
-  const bool window = j >= p.K;
-  const int32_t idx = window ? __ldg(p.swa + (int64_t)t * p.swa_stride + (j - p.K))
-                             : __ldg(p.topk + (int64_t)t * p.topk_stride + j);
-  if (idx < 0) return -1;
-  if (!window && p.topk_length != nullptr && j >= __ldg(p.topk_length + t)) return -1;
-  const int32_t req = __ldg(p.req_id + t);
-  if (req < 0 || req >= p.R) return -1;
-  const bool own = window && p.swa_block_table != nullptr;  // the window scope's own cache
-  const int32_t P = own ? p.swa_P : p.P;
-  const int32_t b = idx / P;
-  const int32_t off = idx - b * P;
-  if (b >= (own ? p.swa_max_blocks : p.max_blocks)) return -1;
-  const int32_t page = own ? __ldg(p.swa_block_table + (int64_t)req * p.swa_bt_stride + b)
-                           : __ldg(p.block_table + (int64_t)req * p.bt_stride + b);
-  if (page < 0 || (int64_t)page >= (own ? p.swa_num_pages : p.num_pages)) return -1;
-  return page * P + off;
+  IndexStep s;
+  if (!index_block(p, t, j, __ldg(index_addr(p, t, j)), __ldg(p.req_id + t), s)) return -1;
+  return index_slot(p, s, __ldg(s.bt_entry));
 }
 
 __global__ void __launch_bounds__(256) convert_kernel(ConvertParams p) {
