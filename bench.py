@@ -19,6 +19,7 @@ timed region is bracketed by barriers and the max time over ranks is reported.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -49,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample length")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=None,
+                    help="split request for the main workload (as num_splits of the C API; default: the workload's)")
     return ap.parse_args(argv)
 
 
@@ -394,6 +397,8 @@ def main(argv=None):
     peaks, src = load_peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     w = synth.WORKLOADS[args.config]
+    if args.num_splits is not None:
+        w = dataclasses.replace(w, max_splits=args.num_splits)
     K = args.steps
     sampler = ClockSampler(local)
     r = measure(api, lib, synth, torch, w, rank_seed(args.config, rank), dev, flush, K, args.warmup,
