@@ -709,28 +709,37 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, const
     ++nerdv;
     tc_fence_after();
     // O^T (lane = latent dim, column = head) leaves by TMA stores, which take no slot in the
-    // load/store pipeline that the gathers keep busy.  Per block of 128 dims and 32 heads the
-    // warp writes its 32 dim-lanes of the 32 heads, scaled, as the box [32 heads][32 dims]
-    // (bf16 or fp32) into one of its two 4 KB staging buffers (a slice of the P^T buffers,
-    // free once O is final, and a slice of the staging region) and one lane stores the box
-    // to out[t, heads, dims] (or o_part[t, split, heads, dims]); the tensor map clips heads
-    // past H.
+    // load/store pipeline that the gathers keep busy.  Per block of 128 dims the warp loads
+    // its 32 dim-lanes of all 64 heads from TMEM (two loads in flight together), scales them
+    // and writes them as [heads][32 dims] boxes into its two alternating 4 KB staging
+    // buffers (a slice of the P^T buffers, free once O is final, and a slice of the staging
+    // region): one box of 64 heads in bf16, or two of 32 heads in fp32; one lane stores each
+    // box to out[t, heads, dims] (or o_part[t, split, heads, dims]), the tensor map clipping
+    // heads past H.
     const int zc = p.S == 1 ? it.t : it.t * p.S + it.split;
     uint8_t* const buf0 = smem + kOffP + warp * kEpiWarpBytes;
     uint8_t* const buf1 = smem + kOffEpi + warp * kEpiWarpBytes;
     const bool odd = lane & 1;
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      const int blk = cc >> 1, h0 = 32 * (cc & 1);
-      uint32_t o[32];
-      tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
-      tmem_wait_ld();
-      if (lane == 0 && cc >= 2) bulk_wait_read<1>();  // the store of block cc - 2 read this buffer
+    int nbox = 0;  // boxes committed by this warp in this item
+    auto next_buffer = [&]() -> uint8_t* {  // once the store two boxes back has read it
+      if (lane == 0 && nbox >= 2) bulk_wait_read<1>();
       __syncwarp();
-      uint8_t* sb = (cc & 1) ? buf1 : buf0;
-      // the 32 heads' factors into registers first: loads interleaved with the staging
-      // stores would be kept in order behind them (they may alias) and serialise the block
-      float fac[32];
+      return (nbox & 1) ? buf1 : buf0;
+    };
+    auto store_box = [&](uint8_t* sb, int x, int y) {
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        // a box wholly past H is not stored, but still closes a (then empty) group, so
+        // that the wait in next_buffer always counts the store of the other buffer
+        if (y < p.H) tma_store_3d(omap, smem_u32(sb), x, y, zc);
+        bulk_commit();
+      }
+      ++nbox;
+    };
+    // the 32 heads' factors from h0 into registers first: loads interleaved with the
+    // staging stores would be kept in order behind them (they may alias) and serialise it
+    auto factors = [&](int h0, float (&fac)[32]) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint4 f4 = ld_shared_v4(smem_u32(&m->factor[fb][h0 + 4 * k]));
@@ -739,29 +748,47 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, const
         fac[4 * k + 2] = __uint_as_float(f4.z);
         fac[4 * k + 3] = __uint_as_float(f4.w);
       }
-      if (p.S == 1) {
-        // lanes 2k and 2k + 1 (dims 2k, 2k + 1) trade one value per pair of heads (i, i + 1),
-        // so that lane 2k stores head i's bf16 pair and lane 2k + 1 head i + 1's
+    };
+    // bf16 rows h0 .. h0+31 of a [64 heads][32 dims] box: lanes 2k and 2k + 1 (dims 2k,
+    // 2k + 1) trade one value per pair of heads (i, i + 1), so that lane 2k stores head
+    // i's bf16 pair and lane 2k + 1 head i + 1's
+    auto stage_bf16 = [&](uint8_t* sb, const uint32_t (&o)[32], int h0) {
+      float fac[32];
+      factors(h0, fac);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float v0 = __uint_as_float(o[i]) * fac[i], v1 = __uint_as_float(o[i + 1]) * fac[i + 1];
-          const float keep = odd ? v1 : v0, give = odd ? v0 : v1;
-          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-          const uint32_t pair = bf16x2_bits(odd ? __floats2bfloat162_rn(got, keep) : __floats2bfloat162_rn(keep, got));
-          *reinterpret_cast<uint32_t*>(sb + (i + (odd ? 1 : 0)) * 64 + (lane & ~1) * 2) = pair;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          *reinterpret_cast<float*>(sb + (i * 32 + lane) * 4) = __uint_as_float(o[i]) * fac[i];
+      for (int i = 0; i < 32; i += 2) {
+        const float v0 = __uint_as_float(o[i]) * fac[i], v1 = __uint_as_float(o[i + 1]) * fac[i + 1];
+        const float keep = odd ? v1 : v0, give = odd ? v0 : v1;
+        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const uint32_t pair = bf16x2_bits(odd ? __floats2bfloat162_rn(got, keep) : __floats2bfloat162_rn(keep, got));
+        *reinterpret_cast<uint32_t*>(sb + (h0 + i + (odd ? 1 : 0)) * 64 + (lane & ~1) * 2) = pair;
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        // a box wholly past H is not stored, but still closes a (then empty) group, so
-        // that the wait above always counts the store of the other buffer
-        if (it.g * kHeads + h0 < p.H) tma_store_3d(omap, smem_u32(sb), blk * 128 + 32 * warp, it.g * kHeads + h0, zc);
-        bulk_commit();
+    };
+    auto stage_f32 = [&](uint8_t* sb, const uint32_t (&o)[32], int h0) {  // a [32 heads][32 dims] box
+      float fac[32];
+      factors(h0, fac);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) *reinterpret_cast<float*>(sb + (i * 32 + lane) * 4) = __uint_as_float(o[i]) * fac[i];
+    };
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      uint32_t oa[32], ob[32];
+      tmem_ld32(tmem + lane_base + kColO + blk * kHeads, oa);       // heads 0-31
+      tmem_ld32(tmem + lane_base + kColO + blk * kHeads + 32, ob);  // heads 32-63
+      tmem_wait_ld();
+      const int x = blk * 128 + 32 * warp, y = it.g * kHeads;
+      if (p.S == 1) {
+        uint8_t* sb = next_buffer();
+        stage_bf16(sb, oa, 0);
+        stage_bf16(sb, ob, 32);
+        store_box(sb, x, y);
+      } else {
+        uint8_t* sb = next_buffer();
+        stage_f32(sb, oa, 0);
+        store_box(sb, x, y);
+        sb = next_buffer();
+        stage_f32(sb, ob, 32);
+        store_box(sb, x, y + 32);
       }
     }
     if (lane == 0) bulk_wait_read<0>();  // the next item writes P^T into the staging
@@ -780,7 +807,7 @@ __device__ void softmax_warps(uint8_t* smem, Misc* m, const AttnParams& p, const
 struct KernelParams {
   AttnParams p;
   CUtensorMap qmap;  // the type carries the 64-byte alignment of a tensor map
-  CUtensorMap omap;  // out [T, H, 512] bf16 (one split) or o_part [T*S, H, 512] fp32, boxes of 32 x 32
+  CUtensorMap omap;  // out [T, H, 512] bf16 (one split) or o_part [T*S, H, 512] fp32
 };
 
 template <bool ALIGN16, int FMT>
@@ -891,7 +918,8 @@ bool make_q_map(const AttnParams& p, CUtensorMap* map) {
 }
 
 // The output as [rows of one token (and split)] x [H heads] x [512 dims], stored by boxes of
-// 32 dims x 32 heads from the epilogue's staging (no swizzle).
+// 32 dims x 64 heads (bf16) or 32 dims x 32 heads (fp32) from the epilogue's staging (no
+// swizzle).
 bool make_out_map(const AttnParams& p, CUtensorMap* map) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
@@ -899,7 +927,7 @@ bool make_out_map(const AttnParams& p, CUtensorMap* map) {
   const cuuint64_t esize = one ? 2 : 4;
   const cuuint64_t gdim[3] = {(cuuint64_t)kLatent, (cuuint64_t)p.H, (cuuint64_t)p.T * (one ? 1 : (cuuint64_t)p.S)};
   const cuuint64_t gstride[2] = {(cuuint64_t)kLatent * esize, (cuuint64_t)p.H * kLatent * esize};
-  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t box[3] = {32, one ? 64u : 32u, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   void* base = one ? p.out : static_cast<void*>(p.o_part);
   return enc(map, one ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, gdim, gstride, box,
