@@ -415,12 +415,18 @@ def main(argv=None):
     # decode, d2h of out + lse, per step (out still holds the device path's result)
     try:
         e2e = run_e2e(api, inp, w, dev, r["stream"], flush, min(args.e2e_steps, K), rows_per_step,
-                      device_out=r["out"])
+                      device_out=r["out"], seed=rank_seed(args.config, rank) + 7)
     except Exception as exc:  # keep the device-timed line; the failure is reported in it
         e2e = {"seconds": None, "steps": 0, "h2d": 0, "d2h": 0, "error": repr(exc)[:300]}
         print(f"e2e leg failed: {exc!r}", file=sys.stderr)
     secs = max_over_ranks(pg, e2e["seconds"] if e2e["seconds"] is not None else float("inf"), dev)
     e2e_val = job_rate(rows_per_step, e2e["steps"], world, secs) if secs != float("inf") else None
+    ssecs = max_over_ranks(pg, e2e.get("serial_seconds") or float("inf"), dev)
+    serial_e2e = None
+    if ssecs != float("inf") and e2e["steps"]:
+        serial_e2e = {"value": job_rate(rows_per_step, e2e["steps"], world, ssecs),
+                      "us_per_step": ssecs / e2e["steps"] * 1e6,
+                      "method": "one stream: copy in, decode, copy out; each step timed alone after an L2 flush"}
 
     # the other target workloads (mid batch, long context; the single-request latency case)
     # measured the same way in the same run, on rank 0's replica only
@@ -462,7 +468,11 @@ def main(argv=None):
         "extra_workloads": extras,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "steps": e2e["steps"], "transfers": "one h2d of the packed inputs, one d2h of out + lse",
+                "steps": e2e["steps"], "transfers": "one h2d of the packed inputs, one d2h of out + lse, per step",
+                "method": "pipelined over three streams (step i+1's copy in and step i-1's copy out overlap "
+                          "step i's decode), two device buffer sets, three rotating input sets (no L2 reuse "
+                          "between consecutive steps); timed from the first copy in to the last copy out",
+                "serial": serial_e2e,
                 "matches_device_path": e2e.get("matches_device_path"), **({"error": e2e["error"]} if "error" in e2e else {})},
         "gpu_launches": K * S_launches,
         "clocks": r["clocks"],
@@ -521,40 +531,84 @@ def pack_views(buf, lay):
     return {k: buf[o:o + n].view(dt).view(shape) for k, (o, n, dt, shape) in lay.items()}
 
 
-def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step, device_out=None):
-    """The step through the public call with host-resident inputs: every step copies the
+def e2e_names(w):
+    """The per-step host inputs of the public call, in packing order."""
+    return [k for k in ("q", "block_table", "req_id", "topk_idx", "swa_idx")
+            if not (k == "topk_idx" and not w.topk) and not (k == "swa_idx" and not w.swa)]
+
+
+def e2e_input_sets(inp, w, n, seed):
+    """n host input sets of the step's shapes: set 0 is the step's own inputs; each other set
+    draws a fresh q and fresh top-k positions in every token's context (the same -1 entries,
+    window and block table), so that consecutive steps of the pipelined leg gather
+    different rows and find nothing of the previous step in L2."""
+    import torch
+    base = {k: getattr(inp, k).cpu() for k in e2e_names(w)}
+    sets = [base]
+    g = torch.Generator().manual_seed(seed)
+    for _ in range(1, n):
+        d = dict(base)
+        d["q"] = torch.randn(base["q"].shape, generator=g).to(torch.bfloat16)
+        if "topk_idx" in d:
+            tk = base["topk_idx"].clone()
+            for t in range(tk.shape[0]):
+                valid = tk[t] >= 0
+                nv = int(valid.sum())
+                if nv:
+                    tk[t, valid] = torch.randperm(int(inp.ctx_lens[t]), generator=g)[:nv].to(torch.int32)
+            d["topk_idx"] = tk
+        sets.append(d)
+    return sets
+
+
+def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step, device_out=None, seed=0):
+    """The step through the public call with host-resident inputs.  Every step copies its
     inputs (packed in one pinned buffer) to the device in one transfer, runs
     sparse_mla_decode on views of that buffer, and reads out and lse (one device buffer)
-    back in one transfer."""
+    back in one transfer.
+
+    Pipelined (the reported value): the copies in, the decode and the copies out run on
+    three streams over two device input and two result buffers, so step i + 1's inputs
+    travel while step i decodes and step i - 1's results come back, as a serving loop
+    would run; the timed region spans all steps from the first copy in to the last copy
+    out.  Three input sets rotate (see e2e_input_sets), so no step finds its rows in L2.
+    Serial (reported beside it): one stream, copy in, decode, copy out, each step timed
+    alone after an L2 flush."""
     import torch
-    names = [k for k in ("q", "block_table", "req_id", "topk_idx", "swa_idx")
-             if not (k == "topk_idx" and not w.topk) and not (k == "swa_idx" and not w.swa)]
-    src = {k: getattr(inp, k).cpu() for k in names}
-    lay_in, nb_in = pack_layout([(k, src[k]) for k in names])
-    h_in = torch.zeros(nb_in, dtype=torch.uint8).pin_memory()
-    for k, v in pack_views(h_in, lay_in).items():
-        v.copy_(src[k])
-    d_in = torch.empty(nb_in, dtype=torch.uint8, device=dev)
-    dbuf = pack_views(d_in, lay_in)
+    names = e2e_names(w)
+    sets = e2e_input_sets(inp, w, 3, seed)
+    lay_in, nb_in = pack_layout([(k, sets[0][k]) for k in names])
+    h_in = []
+    for st in sets:
+        h = torch.zeros(nb_in, dtype=torch.uint8).pin_memory()
+        for k, v in pack_views(h, lay_in).items():
+            v.copy_(st[k])
+        h_in.append(h)
     T, H = w.num_tokens, w.num_heads
     lay_out, nb_out = pack_layout([("out", torch.empty(T, H, 512, dtype=torch.bfloat16)),
                                    ("lse", torch.empty(T, H, dtype=torch.float32))])
-    d_res = torch.empty(nb_out, dtype=torch.uint8, device=dev)
-    res = pack_views(d_res, lay_out)
-    h_res = torch.empty(nb_out, dtype=torch.uint8).pin_memory()
-    dims = api.make_dims(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
-                         dbuf.get("topk_idx"), dbuf.get("swa_idx"), w.block_size)
+    d_in = [torch.empty(nb_in, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dbuf = [pack_views(x, lay_in) for x in d_in]
+    d_res = [torch.empty(nb_out, dtype=torch.uint8, device=dev) for _ in range(2)]
+    res = [pack_views(x, lay_out) for x in d_res]
+    h_res = [torch.empty(nb_out, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    dims = api.make_dims(dbuf[0]["q"], inp.kv_cache, dbuf[0]["block_table"], dbuf[0]["req_id"],
+                         dbuf[0].get("topk_idx"), dbuf[0].get("swa_idx"), w.block_size)
     ws = torch.empty(api.workspace_size(dims, w.max_splits, 0), dtype=torch.uint8, device=dev)
 
-    def one():
-        d_in.copy_(h_in, non_blocking=True)
-        api.sparse_mla_decode(dbuf["q"], inp.kv_cache, dbuf["block_table"], dbuf["req_id"],
-                              dbuf.get("topk_idx"), dbuf.get("swa_idx"), inp.sink, inp.scale,
-                              out=res["out"], lse=res["lse"], num_splits=w.max_splits, workspace=ws,
+    def decode(b):
+        api.sparse_mla_decode(dbuf[b]["q"], inp.kv_cache, dbuf[b]["block_table"], dbuf[b]["req_id"],
+                              dbuf[b].get("topk_idx"), dbuf[b].get("swa_idx"), inp.sink, inp.scale,
+                              out=res[b]["out"], lse=res[b]["lse"], num_splits=w.max_splits, workspace=ws,
                               block_size=w.block_size, stream=stream)
-        h_res.copy_(d_res, non_blocking=True)
 
-    with torch.cuda.stream(stream):  # every copy, call and event on one stream
+    # ---- serial: every copy, call and event on one stream
+    def one():
+        d_in[0].copy_(h_in[0], non_blocking=True)
+        decode(0)
+        h_res[0].copy_(d_res[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
         for _ in range(3):
             one()
         torch.cuda.synchronize()
@@ -565,11 +619,56 @@ def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step, device_out=No
             one()
             b.record(stream)
         torch.cuda.synchronize()
-    secs = sum(a.elapsed_time(b) for a, b in evs) / 1e3
-    r = {"seconds": secs, "steps": steps, "h2d": nb_in, "d2h": nb_out}
+    serial_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    matches = None
     if device_out is not None:  # same inputs, same kernels: the results must agree bit for bit
-        r["matches_device_path"] = bool(torch.equal(pack_views(h_res, lay_out)["out"], device_out.cpu()))
-    return r
+        matches = bool(torch.equal(pack_views(h_res[0], lay_out)["out"], device_out.cpu()))
+
+    # ---- pipelined: copies in on s_in, decode on `stream`, copies out on s_out
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def step(i):
+        b = i & 1
+        if i >= 2:
+            s_in.wait_event(ev_done[b])  # decode i - 2 has read d_in[b]
+        with torch.cuda.stream(s_in):
+            d_in[b].copy_(h_in[i % len(h_in)], non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])  # the copy out of step i - 2 has read d_res[b]
+        decode(b)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            h_res[b].copy_(d_res[b], non_blocking=True)
+        ev_out[b].record(s_out)
+
+    torch.cuda.synchronize()
+    i = 0
+    for _ in range(6):  # warm-up
+        step(i)
+        i += 1
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for _ in range(steps):
+        step(i)
+        i += 1
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    pipe_s = t0.elapsed_time(t1) / 1e3
+    if device_out is not None:  # one more step on set 0: the pipelined path gives the same result
+        while i % len(h_in) != 0:
+            i += 1
+        step(i)
+        torch.cuda.synchronize()
+        matches = bool(matches and torch.equal(pack_views(h_res[i & 1], lay_out)["out"], device_out.cpu()))
+    return {"seconds": pipe_s, "steps": steps, "h2d": nb_in, "d2h": nb_out, "matches_device_path": matches,
+            "serial_seconds": serial_s}
 
 
 if __name__ == "__main__":

@@ -43,3 +43,29 @@ def test_pack_views_round_trip_bit_exact():
 def test_pack_layout_of_empty_list():
     lay, total = bench.pack_layout([])
     assert lay == {} and total == 256
+
+
+def test_e2e_input_sets_keep_the_step_shape_and_draw_new_rows():
+    from sparse_mla_decode_req_gb300 import synth
+    w = synth.small_workload(num_tokens=4, topk=96, swa=32, ctx=300, n_invalid=5)
+    inp = synth.make_inputs(w, seed=11)
+    sets = bench.e2e_input_sets(inp, w, 3, seed=3)
+    assert len(sets) == 3
+    names = bench.e2e_names(w)
+    for k in names:  # set 0 is the step's own inputs
+        assert torch.equal(sets[0][k], getattr(inp, k).cpu())
+    for s in sets[1:]:
+        assert set(s) == set(names)
+        for k in names:
+            assert s[k].shape == sets[0][k].shape and s[k].dtype == sets[0][k].dtype
+        for k in ("block_table", "req_id", "swa_idx"):  # pages and window unchanged
+            assert torch.equal(s[k], sets[0][k])
+        assert not torch.equal(s["q"], sets[0]["q"])
+        tk, tk0 = s["topk_idx"], sets[0]["topk_idx"]
+        assert torch.equal(tk < 0, tk0 < 0)  # the same -1 entries, so the same valid-row count
+        assert not torch.equal(tk, tk0)
+        for t in range(tk.shape[0]):
+            v = tk[t][tk[t] >= 0]
+            assert int(v.min()) >= 0 and int(v.max()) < inp.ctx_lens[t]
+            assert v.unique().numel() == v.numel()  # distinct positions, as the workload draws them
+    assert not torch.equal(sets[1]["topk_idx"], sets[2]["topk_idx"])
