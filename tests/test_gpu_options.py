@@ -6,7 +6,8 @@
 * a per-token top-k length that masks the top-k columns at and past it;
 * compaction: the conversion packs each token's valid slots to the front and the
   attention reads per-token counts instead of masked rows;
-* the pages' ragged conversion with 0 for an invalid entry.
+* the pages' ragged conversion with 0 for an invalid entry;
+* several query tokens per request (multi-token prediction) through req_id.
 
 Integer outputs (slots, counts, ragged output, bf16 rows) are compared bit for bit; the
 attention within the tolerances of the other GPU parity tests.
@@ -21,7 +22,7 @@ from oracle.bf16_cache import dequant_rows_bf16, sparse_mla_decode_bf16
 from oracle.dual_scope import sparse_mla_decode_dual
 from oracle.ragged import apply_topk_length, compact, convert_req_index_ragged
 from sparse_mla_decode_req_gb300 import api, build, synth
-from tests.gpu_util import assert_lse_close, assert_out_close, bf16_to_f64
+from tests.gpu_util import assert_lse_close, assert_out_close, bf16_to_f64, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -124,6 +125,29 @@ def test_decode_bf16_cache_large_batch_sampled():
     ro, rl = _bf16_oracle(inp, cache, toks)
     assert_out_close(out[toks], ro, "bf16 large batch")
     assert_lse_close(lse[toks], rl, "bf16 large batch")
+
+
+@pytest.mark.parametrize("fmt,ns", [("fp8", 1), ("fp8", -3), ("bf16", 1), ("bf16", -2)])
+def test_several_tokens_per_request(fmt, ns):
+    """Several query tokens of one request (multi-token prediction): tokens 2r and 2r + 1
+    both read request 2r's pages through req_id, each with its own top-k list and window;
+    the request rows of the odd tokens go unused."""
+    w = synth.small_workload(num_tokens=6, num_heads=64, topk=150, swa=40, ctx=400, n_invalid=11)
+    inp = synth.make_inputs(w, seed=91, device="cuda")
+    inp.req_id.copy_(torch.tensor([0, 0, 2, 2, 4, 4], dtype=torch.int32))
+    if fmt == "fp8":
+        out, lse = api.sparse_mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.req_id, inp.topk_idx,
+                                         inp.swa_idx, inp.sink, inp.scale, num_splits=ns)
+        torch.cuda.synchronize()
+        ro, rl = oracle_decode(inp)
+    else:
+        cache = synth.make_cache_bf16(inp.num_pages, w.block_size, 93, "cuda")
+        out, lse = api.sparse_mla_decode(inp.q, cache, inp.block_table, inp.req_id, inp.topk_idx, inp.swa_idx,
+                                         inp.sink, inp.scale, num_splits=ns, cache_format=api.CACHE_BF16)
+        torch.cuda.synchronize()
+        ro, rl = _bf16_oracle(inp, cache)
+    assert_out_close(out, ro, f"several tokens per request {fmt}")
+    assert_lse_close(lse, rl, f"several tokens per request {fmt}")
 
 
 # ----------------------------------------------------------------- two caches
