@@ -344,20 +344,11 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Generic-proxy shared-memory writes -> visible to the async proxy (UMMA operand reads).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, f32 accumulate).
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same, issued by one elected lane of a converged warp.  The whole warp runs the issue
-// loop, so its descriptor arithmetic stays warp-uniform (uniform registers) and, unrolled
-// with constant offsets, an MMA issues at the tensor core's pace (a loop run by one
-// divergent lane with per-iteration descriptor math took ~90 cycles per MMA on GB300).
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, f32 accumulate), issued
+// by one elected lane of a converged warp.  The whole warp runs the issue loop, so its
+// descriptor arithmetic stays warp-uniform (uniform registers) and, unrolled with constant
+// offsets, an MMA issues at the tensor core's pace (a loop run by one divergent lane with
+// per-iteration descriptor math took ~90 cycles per MMA on GB300).
 __device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate) {
   asm volatile(
@@ -368,13 +359,9 @@ __device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc, 
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive (once) on `bar` when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-// The same commit from one elected lane of a converged warp (the lane that issued the MMAs
-// with umma_ss_elect: elect.sync picks the same lane for the same member mask).
+// Arrive (once) on `bar` when every MMA issued so far has completed, from one elected lane
+// of a converged warp (the lane that issued the MMAs with umma_ss_elect: elect.sync picks
+// the same lane for the same member mask).
 __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
