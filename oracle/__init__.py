@@ -7,3 +7,4 @@ from .sparse_mla import (  # noqa: F401
     attend, convert_req_index, decode_bf16, decode_e4m3, decode_ue8m0, dequant_rows,
     lse_combine, row_offsets, sparse_mla_decode,
 )
+from .indexer import cp_gather_indexer_k, mqa_logits, topk_positions  # noqa: F401,E402
