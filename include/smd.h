@@ -325,6 +325,83 @@ SMD_API int smd_sparse_mla_decode_static_scratch(const smd_dims *dims, const voi
  */
 SMD_API int smd_read_static_scratch_status(int32_t *device_status, smd_stream_t stream);
 
+/* ------------------------------------------------------------------------------------
+ * The indexer step: the choice of each decode token's top-k positions (the topk_idx of
+ * the decode calls above).
+ *
+ * Indexer key cache.  Position s of a request lives in page block_table[req, s / P] at
+ * in-page position s % P.  A page of layout 0 holds the P positions' head_dim fp8 e4m3
+ * key bytes (P * head_dim bytes), then their P little-endian float32 scales; layout 1
+ * holds each position's head_dim bytes followed by its scale.  A key element is
+ * e4m3(byte) * scale.  (vLLM PR #52212 report, "关键源码片段", the cp-gather kernel of
+ * the indexer cache, which takes a layout switch and separate value and scale pointers;
+ * the pages print neither layout, these are the plainest readings.)
+ * ------------------------------------------------------------------------------------ */
+
+/*
+ * Key gather of a ragged batch (vLLM PR #52212 report, "关键源码片段",
+ * _cp_gather_indexer_quant_cache_gfx950_kernel; "实现拆解" item 4: runtime batch count,
+ * 64-bit block offsets).  For tid in [0, num_tokens): b = token_to_seq[tid]; the token is
+ * skipped (nothing written) unless 0 <= b < num_batches and cu_seqlen[b] <= tid <
+ * cu_seqlen[b + 1]; position pos = tid - cu_seqlen[b] reads block_table[b, pos / P]
+ * (row stride bt_stride); a block at or past max_blocks or a page outside [0, num_pages)
+ * writes scale_out[tid] = 0 and leaves k_out[tid] as it is; otherwise k_out[tid, :] =
+ * the position's head_dim key bytes and scale_out[tid] = its scale.
+ * cache u8 [num_pages, P * (head_dim + 4)], 16-byte aligned; block_table int32;
+ * cu_seqlen int32 [num_batches + 1]; token_to_seq int32 [num_tokens]; k_out u8
+ * [num_tokens, head_dim] and scale_out f32 [num_tokens], 4-byte aligned.
+ * head_dim: a multiple of 4 in [4, 4096]; layout 0 or 1.
+ */
+SMD_API int smd_indexer_gather_k(const uint8_t *cache, int64_t num_pages, int32_t block_size, int32_t head_dim,
+                                 int32_t layout, const int32_t *block_table, int32_t num_batches,
+                                 int32_t max_blocks, int64_t bt_stride, const int32_t *cu_seqlen,
+                                 const int32_t *token_to_seq, int32_t num_tokens, uint8_t *k_out, float *scale_out,
+                                 smd_stream_t stream);
+
+/* Shape of an indexer logits call. */
+typedef struct smd_indexer_dims {
+  int32_t num_tokens;          /* T query tokens (one per request, or several sharing one) */
+  int32_t num_heads;           /* H indexer heads: 32, 64 or 128 */
+  int32_t head_dim;            /* 128 */
+  int32_t num_requests;        /* R rows of block_table */
+  int32_t max_blocks_per_req;  /* W used columns of block_table */
+  int32_t block_size;          /* P positions per page: 8, 16, 32, 64 or 128 */
+  int64_t num_pages;
+  int64_t bt_stride;           /* row stride of block_table, >= W */
+  int32_t max_len;             /* L: logits row length (positions per token) */
+  int32_t layout;              /* key cache layout: 0 */
+} smd_indexer_dims;
+
+/*
+ * fp8 paged MQA logits (vLLM PR #41217 report, "实现拆解" item 6: per-head scores and
+ * their weighted sum in one kernel; "关键源码片段", SparseAttnIndexer.forward: per-head
+ * weights projected beside the key).  For token t of request r = req_id[t] and position
+ * s < min(ctx_lens[t], L):
+ *   logits[t, s] = sum_h weights[t, h] * max(0, sum_d e4m3(q[t, h, d]) * k_s[d])
+ * (k_s = the position's key, its bytes times its scale; the rectifier is the reading of
+ * the per-head stage, see the design notes).  A position at or past the context, of a
+ * block at or past W, of a page outside [0, num_pages) or of a request outside [0, R)
+ * gets -inf; every entry of the [T, L] row-major logits array is written.
+ * q u8 e4m3 [T, H, 128] and cache (layout 0) 16-byte aligned; weights f32 [T, H];
+ * logits f32 [T, L] 16-byte aligned; device_status (optional) gets bit 0 if a bounded
+ * wait gave up (it is not cleared; zero it before the call).  Tensor cores:
+ * tcgen05.mma kind::f8f6f4, one CTA per token and 128 positions.
+ */
+SMD_API int smd_indexer_mqa_logits(const smd_indexer_dims *dims, const uint8_t *q, const float *weights,
+                                   const uint8_t *cache, const int32_t *block_table, const int32_t *req_id,
+                                   const int32_t *ctx_lens, float *logits, int32_t *device_status,
+                                   smd_stream_t stream);
+
+/*
+ * Top-k positions per token: topk[t, :] = the k positions s < min(ctx_lens[t], max_len)
+ * of the largest finite logits[t, s] (row stride logits_stride >= max_len), those above
+ * the k-th largest value first in ascending position, then the lowest positions equal
+ * to it; -1 pads a token with fewer than k finite logits.  -inf and NaN are never
+ * chosen.  topk int32 [num_tokens, k].  1 <= k <= 2^20.
+ */
+SMD_API int smd_indexer_topk(const float *logits, int32_t num_tokens, int32_t max_len, int64_t logits_stride,
+                             const int32_t *ctx_lens, int32_t k, int32_t *topk, smd_stream_t stream);
+
 /*
  * Test and fault-injection hook (not part of the decode semantics): sets the bound, in
  * nanoseconds of wall time, of every pipeline wait inside the attention kernel for launches

@@ -55,6 +55,23 @@ class Dims(ctypes.Structure):
     ]
 
 
+class IndexerDims(ctypes.Structure):
+    """``smd_indexer_dims`` (include/smd.h)."""
+
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("num_requests", ctypes.c_int32),
+        ("max_blocks_per_req", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64),
+        ("bt_stride", ctypes.c_int64),
+        ("max_len", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
+    ]
+
+
 class DecodeOpts(ctypes.Structure):
     """``smd_decode_opts`` (include/smd.h)."""
 
@@ -97,6 +114,12 @@ _SIGS = {
                                                             ctypes.c_float, _P, _P, ctypes.c_int, _P]),
     "smd_read_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "smd_read_static_scratch_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _P]),
+    "smd_indexer_gather_k": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _P, _P, ctypes.c_int32,
+                                            _P, _P, _P]),
+    "smd_indexer_mqa_logits": (ctypes.c_int, [ctypes.POINTER(IndexerDims), _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "smd_indexer_topk": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _P, ctypes.c_int32,
+                                        _P, _P]),
     "smd_last_error": (ctypes.c_char_p, []),
     "smd_version": (ctypes.c_int, []),
 }
@@ -409,3 +432,54 @@ def set_wait_limit_ns(limit_ns: int) -> int:
     """Bound of the attention kernel's pipeline waits for later launches (0 = default 2 s);
     returns the previous bound.  A test hook: a tiny bound makes the waits give up."""
     return int(load().smd_set_wait_limit_ns(ctypes.c_uint64(int(limit_ns))))
+
+
+# ---------------------------------------------------------------------- indexer step
+def indexer_gather_k(cache, block_table, cu_seqlen, token_to_seq, num_batches: int, block_size: int,
+                     head_dim: int, layout: int = 0, k_out=None, scale_out=None, stream=None):
+    """Key gather of a ragged batch (smd_indexer_gather_k); returns (k u8 [n, head_dim],
+    scale f32 [n]).  Entries the rule does not write keep the contents of k_out /
+    scale_out (fresh buffers start as zeros)."""
+    n = int(token_to_seq.shape[0])
+    dev = cache.device
+    if k_out is None:
+        k_out = torch.zeros(n, head_dim, dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.zeros(n, dtype=torch.float32, device=dev)
+    assert cache.is_contiguous() and k_out.is_contiguous() and scale_out.is_contiguous()
+    W = int(block_table.shape[1])
+    _check(load().smd_indexer_gather_k(
+        _ptr(cache), int(cache.shape[0]), int(block_size), int(head_dim), int(layout), _ptr(block_table),
+        int(num_batches), W, _row_stride(block_table, W), _ptr(cu_seqlen), _ptr(token_to_seq), n,
+        _ptr(k_out), _ptr(scale_out), _stream(stream)))
+    return k_out, scale_out
+
+
+def indexer_mqa_logits(q, weights, cache, block_table, req_id, ctx_lens, max_len: int, block_size: int = 64,
+                       logits=None, status=None, stream=None):
+    """fp8 paged MQA logits (smd_indexer_mqa_logits): q u8 e4m3 [T, H, 128], weights f32
+    [T, H], cache u8 [pages, P * 132] (layout 0); returns logits f32 [T, max_len]."""
+    T, H, D = (int(x) for x in q.shape)
+    R, W = (int(x) for x in block_table.shape)
+    if logits is None:
+        logits = torch.empty(T, max_len, dtype=torch.float32, device=q.device)
+    for name, t in (("q", q), ("weights", weights), ("cache", cache), ("logits", logits)):
+        assert t.is_contiguous(), f"{name} must be contiguous"
+    dims = IndexerDims(T, H, D, R, W, int(block_size), int(cache.shape[0]), _row_stride(block_table, W),
+                       int(max_len), 0)
+    _check(load().smd_indexer_mqa_logits(
+        ctypes.byref(dims), _ptr(q), _ptr(weights), _ptr(cache), _ptr(block_table), _ptr(req_id), _ptr(ctx_lens),
+        _ptr(logits), _ptr(status), _stream(stream)))
+    return logits
+
+
+def indexer_topk(logits, ctx_lens, k: int, out=None, stream=None):
+    """Top-k positions per token (smd_indexer_topk); returns int32 [T, k], -1 padded."""
+    T, L = (int(x) for x in logits.shape)
+    assert logits.stride(1) == 1, "logits: unit column stride"
+    if out is None:
+        out = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    assert out.is_contiguous()
+    _check(load().smd_indexer_topk(_ptr(logits), T, L, int(logits.stride(0)), _ptr(ctx_lens), int(k), _ptr(out),
+                                   _stream(stream)))
+    return out

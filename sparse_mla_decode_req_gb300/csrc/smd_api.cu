@@ -463,6 +463,78 @@ SMD_API int smd_sparse_mla_attention(const smd_dims* dims, const smd_decode_opts
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "attention launch");
 }
 
+SMD_API int smd_indexer_gather_k(const uint8_t* cache, int64_t num_pages, int32_t block_size, int32_t head_dim,
+                                 int32_t layout, const int32_t* block_table, int32_t num_batches,
+                                 int32_t max_blocks, int64_t bt_stride, const int32_t* cu_seqlen,
+                                 const int32_t* token_to_seq, int32_t num_tokens, uint8_t* k_out, float* scale_out,
+                                 smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (num_tokens < 0) return fail(SMD_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return SMD_OK;
+  if (head_dim < 4 || head_dim > 4096 || head_dim % 4 != 0)
+    return fail(SMD_ERR_INVALID_ARG, "head_dim %d: a multiple of 4 in [4, 4096]", head_dim);
+  if (layout != 0 && layout != 1) return fail(SMD_ERR_INVALID_ARG, "layout %d is not 0 or 1", layout);
+  if (block_size < 1 || num_pages < 1 || num_batches < 0 || max_blocks < 1 || bt_stride < max_blocks)
+    return fail(SMD_ERR_INVALID_ARG, "bad block_size/num_pages/num_batches/max_blocks/bt_stride");
+  if (num_pages > INT32_MAX) return fail(SMD_ERR_INVALID_ARG, "num_pages above 2^31 - 1");
+  if (cache == nullptr || block_table == nullptr || cu_seqlen == nullptr || token_to_seq == nullptr ||
+      k_out == nullptr || scale_out == nullptr)
+    return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(cache)) return fail(SMD_ERR_INVALID_ARG, "cache not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(k_out) & 3u) || (reinterpret_cast<uintptr_t>(scale_out) & 3u))
+    return fail(SMD_ERR_INVALID_ARG, "k_out/scale_out not 4-byte aligned");
+  smd::IndexerGatherParams p{cache, block_table, cu_seqlen, token_to_seq, k_out, scale_out, bt_stride,
+                             num_tokens, num_batches, max_blocks, block_size, head_dim, layout, (int32_t)num_pages};
+  const cudaError_t e = smd::launch_indexer_gather(p, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "indexer gather launch");
+}
+
+SMD_API int smd_indexer_mqa_logits(const smd_indexer_dims* d, const uint8_t* q, const float* weights,
+                                   const uint8_t* cache, const int32_t* block_table, const int32_t* req_id,
+                                   const int32_t* ctx_lens, float* logits, int32_t* device_status,
+                                   smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (d == nullptr) return fail(SMD_ERR_INVALID_ARG, "dims is NULL");
+  if (d->num_tokens < 0 || d->num_tokens > kMaxTokens)
+    return fail(SMD_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", d->num_tokens, kMaxTokens);
+  if (d->head_dim != 128) return fail(SMD_ERR_UNSUPPORTED, "head_dim %d: the logits kernel takes 128", d->head_dim);
+  if (d->num_heads != 32 && d->num_heads != 64 && d->num_heads != 128)
+    return fail(SMD_ERR_UNSUPPORTED, "num_heads %d: the logits kernel takes 32, 64 or 128", d->num_heads);
+  const int32_t P = d->block_size;
+  if (P < 8 || P > 128 || (P & (P - 1)) != 0)
+    return fail(SMD_ERR_UNSUPPORTED, "block_size %d: the logits kernel takes 8, 16, 32, 64 or 128", P);
+  if (d->layout != 0) return fail(SMD_ERR_UNSUPPORTED, "layout %d: the logits kernel reads layout 0", d->layout);
+  if (d->num_requests < 1 || d->max_blocks_per_req < 1 || d->bt_stride < d->max_blocks_per_req || d->num_pages < 1)
+    return fail(SMD_ERR_INVALID_ARG, "bad num_requests/max_blocks_per_req/bt_stride/num_pages");
+  if (d->num_pages > INT32_MAX) return fail(SMD_ERR_INVALID_ARG, "num_pages above 2^31 - 1");
+  if (d->max_len < 0) return fail(SMD_ERR_INVALID_ARG, "max_len %d < 0", d->max_len);
+  if (d->num_tokens == 0 || d->max_len == 0) return SMD_OK;
+  if (q == nullptr || weights == nullptr || cache == nullptr || block_table == nullptr || req_id == nullptr ||
+      ctx_lens == nullptr || logits == nullptr)
+    return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(q) || !aligned16(cache) || !aligned16(logits))
+    return fail(SMD_ERR_INVALID_ARG, "q/cache/logits not 16-byte aligned");
+  smd::IndexerLogitsParams p{q, weights, cache, block_table, req_id, ctx_lens, logits,
+                             reinterpret_cast<uint32_t*>(device_status), d->bt_stride, d->num_tokens, d->num_heads,
+                             P, d->num_requests, d->max_blocks_per_req, d->max_len, (int32_t)d->num_pages,
+                             smd::wait_limit_ns()};
+  const cudaError_t e = smd::launch_indexer_logits(p, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "indexer logits launch");
+}
+
+SMD_API int smd_indexer_topk(const float* logits, int32_t num_tokens, int32_t max_len, int64_t logits_stride,
+                             const int32_t* ctx_lens, int32_t k, int32_t* topk, smd_stream_t stream) {
+  g_err[0] = '\0';
+  if (num_tokens < 0 || max_len < 0 || logits_stride < max_len)
+    return fail(SMD_ERR_INVALID_ARG, "bad num_tokens/max_len/logits_stride");
+  if (k < 1 || k > (1 << 20)) return fail(SMD_ERR_INVALID_ARG, "k %d outside [1, 2^20]", k);
+  if (num_tokens == 0) return SMD_OK;
+  if (logits == nullptr || ctx_lens == nullptr || topk == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
+  smd::IndexerTopkParams p{logits, ctx_lens, topk, logits_stride, num_tokens, max_len, k};
+  const cudaError_t e = smd::launch_indexer_topk(p, stream);
+  return e == cudaSuccess ? SMD_OK : cuda_fail(e, "indexer top-k launch");
+}
+
 SMD_API int smd_read_status(const void* workspace, int32_t* device_status, smd_stream_t stream) {
   g_err[0] = '\0';
   if (workspace == nullptr || device_status == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");

@@ -108,6 +108,43 @@ int attn_ctas(int64_t items, int sms);
 // Bound of the kernels' pipeline waits (a test hook can shorten it), default 2 s.
 uint64_t wait_limit_ns();
 
+// ---- indexer step (the step that picks each decode token's top-k positions)
+struct IndexerGatherParams {
+  const uint8_t* cache;          // [num_pages, P * (D + 4)]
+  const int32_t* block_table;    // [B, W], row stride bt_stride
+  const int32_t* cu_seqlen;      // [B + 1]
+  const int32_t* token_to_seq;   // [n]
+  uint8_t* k_out;                // [n, D]
+  float* scale_out;              // [n]
+  int64_t bt_stride;
+  int32_t n, B, W, P, D, layout, num_pages;
+};
+cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s);
+
+struct IndexerLogitsParams {
+  const uint8_t* q;              // e4m3 [T, H, 128]
+  const float* weights;          // [T, H]
+  const uint8_t* cache;          // [num_pages, P * 132], layout 0
+  const int32_t* block_table;    // [R, W], row stride bt_stride
+  const int32_t* req_id;         // [T]
+  const int32_t* ctx_lens;       // [T]
+  float* logits;                 // [T, L], row stride L
+  uint32_t* status;              // optional device status word (bit 0: a wait gave up)
+  int64_t bt_stride;
+  int32_t T, H, P, R, W, L, num_pages;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_indexer_logits(const IndexerLogitsParams& p, cudaStream_t s);
+
+struct IndexerTopkParams {
+  const float* logits;           // [T, L], row stride stride
+  const int32_t* ctx_lens;       // [T]
+  int32_t* topk;                 // [T, K]
+  int64_t stride;
+  int32_t T, L, K;
+};
+cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s);
+
 // Sets the thread-local message returned by smd_last_error() and returns `code`.
 int set_error(int code, const char* fmt, ...);
 

@@ -215,3 +215,45 @@ def test_static_scratch_status_before_any_call(lib):
 
 def test_version(lib):
     assert lib.smd_version() >= 100
+
+
+def _idims(T=4, H=64, D=128, R=4, W=16, P=64, pages=64, L=1024, layout=0):
+    return api.IndexerDims(num_tokens=T, num_heads=H, head_dim=D, num_requests=R, max_blocks_per_req=W,
+                           block_size=P, num_pages=pages, bt_stride=W, max_len=L, layout=layout)
+
+
+def test_indexer_logits_rejects_shapes_it_does_not_cover(lib):
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    def call(d):
+        return lib.smd_indexer_mqa_logits(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, None, None)
+    assert call(_idims(D=64)) == api.SMD_ERR_UNSUPPORTED
+    assert call(_idims(H=48)) == api.SMD_ERR_UNSUPPORTED
+    for P in (1, 4, 24, 256):
+        assert call(_idims(P=P)) == api.SMD_ERR_UNSUPPORTED, P
+    assert call(_idims(layout=1)) == api.SMD_ERR_UNSUPPORTED
+    assert call(_idims(T=-1)) == api.SMD_ERR_INVALID_ARG
+    assert call(_idims(L=-1)) == api.SMD_ERR_INVALID_ARG
+    d = _idims()
+    d.bt_stride = 3
+    assert call(d) == api.SMD_ERR_INVALID_ARG
+    assert call(_idims(T=0)) == api.SMD_OK and call(_idims(L=0)) == api.SMD_OK   # nothing to do
+    null = lib.smd_indexer_mqa_logits(ctypes.byref(_idims()), None, fake, fake, fake, fake, fake, fake, None, None)
+    assert null == api.SMD_ERR_INVALID_ARG
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.smd_indexer_mqa_logits(ctypes.byref(_idims()), mis, fake, fake, fake, fake, fake, fake, None,
+                                      None) == api.SMD_ERR_INVALID_ARG
+
+
+def test_indexer_gather_and_topk_validate_arguments(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    def gather(D=128, layout=0, n=8, cache=fake, k_out=fake):
+        return lib.smd_indexer_gather_k(cache, 64, 64, D, layout, fake, 2, 16, 16, fake, fake, n, k_out, fake, None)
+    assert gather(D=6) == api.SMD_ERR_INVALID_ARG
+    assert gather(layout=2) == api.SMD_ERR_INVALID_ARG
+    assert gather(cache=ctypes.c_void_p((1 << 20) + 8)) == api.SMD_ERR_INVALID_ARG
+    assert gather(k_out=ctypes.c_void_p((1 << 20) + 2)) == api.SMD_ERR_INVALID_ARG
+    assert gather(n=0) == api.SMD_OK
+    assert lib.smd_indexer_topk(fake, 4, 100, 100, fake, 0, fake, None) == api.SMD_ERR_INVALID_ARG
+    assert lib.smd_indexer_topk(fake, 4, 100, 99, fake, 8, fake, None) == api.SMD_ERR_INVALID_ARG
+    assert lib.smd_indexer_topk(None, 4, 100, 100, fake, 8, fake, None) == api.SMD_ERR_INVALID_ARG
+    assert lib.smd_indexer_topk(fake, 0, 100, 100, fake, 8, fake, None) == api.SMD_OK
