@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample length")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--indexer-steps", type=int, default=100,
+                    help="steps of the indexer workloads (logits + top-k) measured in the same run; 0 skips them")
     ap.add_argument("--num-splits", type=int, default=None,
                     help="split request for the main workload (as num_splits of the C API; default: the workload's)")
     return ap.parse_args(argv)
@@ -353,6 +355,59 @@ def measure(api, lib, synth, torch, w, seed, dev, flush, K: int, W: int, KP: int
             "comb_ms": [e[2].elapsed_time(e[3]) for e in evk], "out": out, "stream": stream}
 
 
+def measure_indexer(api, torch, si, wi, dev, flush, steps: int, peaks: dict, src: str) -> dict:
+    """The indexer step on one of its workloads: `steps` pairs of launches (fp8 paged MQA
+    logits, then top-k), L2 flushed before each pair, CUDA events around each launch on the
+    launching stream.  The logits kernel's roofline: per position its 128 key bytes and
+    float32 scale from HBM, plus the query heads, weights and the float32 logits row, at
+    the measured copy bandwidth (2 * 128 * H flops per position sit far below the fp8
+    tensor ridge)."""
+    inp = si.make_indexer_inputs(wi, device=dev)
+    T, H, D, K = wi.num_tokens, wi.num_heads, wi.head_dim, wi.topk
+    L = inp.max_len
+    logits = torch.empty(T, L, dtype=torch.float32, device=dev)
+    topk = torch.empty(T, K, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(3 + steps):
+            flush.zero_()
+            e = ev[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            api.indexer_mqa_logits(inp.q, inp.weights, inp.cache, inp.block_table, inp.req_id, inp.ctx_lens, L,
+                                   block_size=wi.block_size, logits=logits, stream=stream)
+            if e:
+                e[1].record(stream)
+            api.indexer_topk(logits, inp.ctx_lens, K, out=topk, stream=stream)
+            if e:
+                e[2].record(stream)
+        torch.cuda.synchronize()
+    lg_us = [a.elapsed_time(b) * 1e3 for a, b, _ in ev]
+    tk_us = [b.elapsed_time(c) * 1e3 for _, b, c in ev]
+    positions = int(sum(inp.ctx))
+    key_bytes = positions * (D + 4)
+    alg = key_bytes + T * H * D + T * H * 4 + T * L * 4
+    flops = 2.0 * H * D * positions
+    lg_s = statistics.mean(lg_us) / 1e6
+    gbs = alg / lg_s / 1e9
+    del inp, logits, topk
+    return {
+        "workload": wi.name, "tokens": T, "heads": H, "head_dim": D, "topk": K, "positions": positions,
+        "max_len": L, "steps": steps,
+        "logits_us": {"mean": statistics.mean(lg_us), "median": statistics.median(lg_us)},
+        "topk_us": {"mean": statistics.mean(tk_us), "median": statistics.median(tk_us)},
+        "positions_per_s": positions / ((statistics.median(lg_us) + statistics.median(tk_us)) / 1e6),
+        "roofline_logits": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": alg,
+                            "key_bytes_per_launch": key_bytes,
+                            "tensor_tflops_achieved": flops / lg_s / 1e12,
+                            "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else "fallback",
+                            "kernel": "smd::indexer_logits_kernel"},
+        "timing": "events around each launch, L2 flushed before each logits + top-k pair",
+    }
+
+
 def summary(w, r, peaks, src) -> dict:
     """Per-workload numbers shared by the headline and the extra workloads."""
     inp, S = r["inp"], r["S"]
@@ -442,6 +497,14 @@ def main(argv=None):
             del re_
             torch.cuda.empty_cache()
 
+    # the indexer step (the top-k source of the decode) on its two workloads
+    indexer = {}
+    if rank == 0 and world == 1 and args.indexer_steps > 0:
+        from sparse_mla_decode_req_gb300 import synth_indexer as si
+        for wi in si.INDEXER_WORKLOADS:
+            indexer[wi.name] = measure_indexer(api, torch, si, wi, dev, flush, args.indexer_steps, peaks, src)
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, el, steps_done, rows_done, cores = cpu_oracle_rate(inp, args.cpu_seconds)
@@ -466,6 +529,7 @@ def main(argv=None):
                               "timing": f"{min(K, 200)} staged steps with events between the kernels "
                                         "(no launch overlap)"},
         "extra_workloads": extras,
+        "indexer": indexer,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e["steps"], "transfers": "one h2d of the packed inputs, one d2h of out + lse, per step",

@@ -67,42 +67,64 @@ __global__ void __launch_bounds__(kGatherThreads) indexer_gather_kernel(IndexerG
 }
 
 // ------------------------------------------------------------------ paged MQA logits
-constexpr int kLgRows = 128;       // positions per CTA (UMMA M)
-constexpr int kLgDim = 128;        // key / query bytes per row (one 128-byte swizzled row)
-constexpr int kLgThreads = 128;
-constexpr uint32_t kLgKBytes = kLgRows * kLgDim;           // 16 KB key tile
-constexpr uint64_t kLgDrainLimitNs = 2000000000ull;
+constexpr int kLgRows = 128;        // positions per tile (UMMA M)
+constexpr int kLgDim = 128;         // key / query bytes per row (one 128-byte swizzled row)
+constexpr int kLgMaxTilesPerCta = 8;  // tiles of one token per CTA, at most (the launch picks 1..8)
+constexpr int kLgStages = 4;        // key tiles in flight per CTA
+constexpr int kLgThreads = 192;     // warps 0-3 epilogue (one TMEM lane quarter each), 4 TMA, 5 MMA
+constexpr int kLgTmaWarp = 4, kLgMmaWarp = 5;
+constexpr uint32_t kLgKBytes = kLgRows * kLgDim;  // 16 KB key tile
 
 __host__ __device__ constexpr uint32_t lg_smem_used(int H) {
-  return kLgKBytes + (uint32_t)H * kLgDim + (uint32_t)H * 4 + 64;
+  return kLgStages * kLgKBytes + (uint32_t)H * kLgDim + (uint32_t)H * 4 + 256;
 }
 
 struct LogitsKernelParams {
   IndexerLogitsParams p;
+  int tiles_per_cta;
   CUtensorMap kmap;   // key bytes of layout 0: [num_pages][P positions][128 bytes], 128B swizzle
   CUtensorMap qmap;   // q: [T * H rows][128 bytes], 128B swizzle
 };
 
+struct LgBars {
+  uint64_t full[kLgStages];   // TMA -> MMA: key tile landed
+  uint64_t empty[kLgStages];  // MMA commit -> TMA: key tile read
+  uint64_t tfull[2];          // MMA commit -> epilogue: scores in TMEM buffer
+  uint64_t tempty[2];         // epilogue (4 warps) -> MMA: TMEM buffer read
+  uint64_t qfull;             // the token's query heads landed
+  uint64_t drain;             // MMA warp's own UMMAs, before TMEM is freed
+  uint32_t tmem;
+  uint32_t abort;
+};
+
+// One CTA per (token, 8 tiles of 128 positions): a TMA warp streams the key tiles through
+// a 4-stage ring, an MMA warp scores each tile against the token's H query heads into one
+// of two TMEM buffers (four kind::f8f6f4 UMMAs of K = 32 bytes), and four epilogue warps
+// turn each buffer into 128 logits while the next tile is scored.
 template <int H>
 __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid_constant__ LogitsKernelParams kp) {
   const IndexerLogitsParams& p = kp.p;
   const int t = blockIdx.y;
-  const int pos0 = blockIdx.x * kLgRows;
+  const int tpc = kp.tiles_per_cta;
+  const int tile0 = blockIdx.x * tpc;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pos = pos0 + tid;
   float* const out = p.logits + (int64_t)t * p.L;
   const int ctx = min(__ldg(p.ctx_lens + t), p.L);
-  if (pos0 >= ctx) {  // a tile wholly past the context: -inf only
-    if (pos < p.L) out[pos] = -INFINITY;
+  const int ntiles = min(tpc, (ctx + kLgRows - 1) / kLgRows - tile0);  // tiles with positions < ctx
+  if (ntiles <= 0) {  // every position of the CTA is past the context: -inf only
+    for (int i = tid; i < tpc * kLgRows; i += kLgThreads) {
+      const int pos = tile0 * kLgRows + i;
+      if (pos < p.L) out[pos] = -INFINITY;
+    }
     return;
   }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* const sK = smem;                                  // [128 positions][128 B], swizzled
-  uint8_t* const sQ = smem + kLgKBytes;                      // [H heads][128 B], swizzled
+  uint8_t* const sK = smem;                                   // kLgStages x [128 positions][128 B]
+  uint8_t* const sQ = smem + kLgStages * kLgKBytes;           // [H heads][128 B] (1 KB aligned)
   float* const sW = reinterpret_cast<float*>(sQ + H * kLgDim);
-  uint64_t* const bar = reinterpret_cast<uint64_t*>(sW + H);  // [0]: tile landed, [1]: MMAs done
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  LgBars* const bars = reinterpret_cast<LgBars*>(sW + H);
+  const uint64_t limit = p.wait_limit_ns;
 
   const int32_t r = __ldg(p.req_id + t);
   const bool req_ok = r >= 0 && r < p.R;
@@ -113,72 +135,140 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
     const int32_t pg = __ldg(p.block_table + (int64_t)r * p.bt_stride + blk);
     return pg >= 0 && pg < p.num_pages ? pg : -1;
   };
-  // this thread's position: its page and float32 scale (layout 0: after the page's key bytes)
-  const int32_t my_page = pos < ctx ? page_of(pos) : -1;
-  float my_scale = 0.f;
-  if (my_page >= 0)
-    my_scale = __ldg(reinterpret_cast<const float*>(p.cache + (int64_t)my_page * p.P * (kLgDim + 4) +
-                                                    (int64_t)p.P * kLgDim + 4 * (pos % p.P)));
   if (tid < H) sW[tid] = __ldg(p.weights + (int64_t)t * H + tid);
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int i = 0; i < kLgStages; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tfull[i], 1);
+      mbar_init(&bars->tempty[i], 4);
+    }
+    mbar_init(&bars->qfull, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, H);
+    tmem_alloc(&bars->tmem, 2 * H);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = bars->tmem;
+  auto give_up = [&]() {
+    atomicExch(&bars->abort, 1u);
+    if (p.status != nullptr) atomicOr(p.status, kStatusTimeout);
+  };
+  auto aborted_ = [&]() { return *reinterpret_cast<volatile uint32_t*>(&bars->abort) != 0u; };
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {  // bounded, warp-uniform
+    bool ok = true;
+    if (!mbar_test(bar, parity)) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar, parity)) {
+        if (aborted_() || globaltimer_ns() - t0 > limit) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    return __all_sync(0xffffffffu, ok);
+  };
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar[0], kLgKBytes + H * kLgDim);
-    // one box per page of the tile (P divides 128); an invalid page reads as zeros
-    for (int j = 0; j < kLgRows / p.P; ++j)
-      tma_load_3d(smem_u32(sK) + j * p.P * kLgDim, &kp.kmap, 0, 0, page_of(pos0 + j * p.P), &bar[0]);
-    tma_load_2d(smem_u32(sQ), &kp.qmap, 0, t * H, &bar[0]);
-  }
-  bool ok = true;
-  if (warp == 0) {
-    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[0], 0, p.wait_limit_ns));
-    if (ok) {
+  if (warp == kLgTmaWarp) {
+    int issued = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->qfull, H * kLgDim);
+      tma_load_2d(smem_u32(sQ), &kp.qmap, 0, t * H, &bars->qfull);
+    }
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % kLgStages;
+      if (i >= kLgStages && !wait(&bars->empty[s], ((i / kLgStages) - 1) & 1)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      if (lane == 0) {
+        const int pos0 = (tile0 + i) * kLgRows;
+        mbar_arrive_expect_tx(&bars->full[s], kLgKBytes);
+        // one box per page of the tile (P divides 128); an invalid page reads as zeros
+        for (int j = 0; j < kLgRows / p.P; ++j)
+          tma_load_3d(smem_u32(sK + s * kLgKBytes) + j * p.P * kLgDim, &kp.kmap, 0, 0, page_of(pos0 + j * p.P),
+                      &bars->full[s]);
+      }
+      __syncwarp();
+      ++issued;
+    }
+    // every key tile issued has landed before the CTA may leave
+    if (lane == 0)
+      for (int i = issued - kLgStages < 0 ? 0 : issued - kLgStages; i < issued; ++i)
+        (void)mbar_wait_bounded(&bars->full[i % kLgStages], (i / kLgStages) & 1, 2000000000ull);
+    if (lane == 0) (void)mbar_wait_bounded(&bars->qfull, 0, 2000000000ull);
+    __syncwarp();
+  } else if (warp == kLgMmaWarp) {
+    const uint64_t db = desc_sw128(smem_u32(sQ), 16, 1024);  // B: query heads, K-major
+    constexpr uint32_t kId = idesc_e4m3_f32(kLgRows, H);
+    bool ok = wait(&bars->qfull, 0);
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int s = i % kLgStages, b = i & 1;
+      ok = wait(&bars->full[s], (i / kLgStages) & 1);
+      ok = ok && (i < 2 || wait(&bars->tempty[b], ((i >> 1) - 1) & 1));
+      if (!ok) break;
       tc_fence_after();
-      const uint64_t da = desc_sw128(smem_u32(sK), 16, 1024);  // A: keys, K-major
-      const uint64_t db = desc_sw128(smem_u32(sQ), 16, 1024);  // B: query heads, K-major
-      constexpr uint32_t kId = idesc_e4m3_f32(kLgRows, H);
+      const uint64_t da = desc_sw128(smem_u32(sK + s * kLgKBytes), 16, 1024);  // A: keys, K-major
 #pragma unroll
       for (int kk = 0; kk < kLgDim / 32; ++kk)  // 32 bytes per step: +2 in the descriptors' 16-byte units
-        umma_f8_elect(tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), kId, kk > 0 ? 1u : 0u);
-      umma_commit_elect(&bar[1]);
-    } else if (lane == 0) {
-      if (p.status != nullptr) atomicOr(p.status, kStatusTimeout);
-      (void)mbar_wait_bounded(&bar[0], 0, kLgDrainLimitNs);  // no TMA write may outlive the CTA
+        umma_f8_elect(tmem + b * H, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), kId, kk > 0 ? 1u : 0u);
+      umma_commit_elect(&bars->empty[s]);
+      umma_commit_elect(&bars->tfull[b]);
     }
-  }
-  ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[1], 0, p.wait_limit_ns));
-  if (ok) {
-    tc_fence_after();
-    float acc = 0.f;
+    if (!ok && lane == 0) give_up();
+    // every UMMA issued has completed before TMEM is freed
+    umma_commit_elect(&bars->drain);
+    if (lane == 0) (void)mbar_wait_bounded(&bars->drain, 0, 2000000000ull);
+    __syncwarp();
+  } else {  // epilogue warps 0-3: warp w owns TMEM lanes (positions) 32w .. 32w+31
+    for (int i = 0; i < ntiles; ++i) {
+      const int b = i & 1;
+      const int pos = (tile0 + i) * kLgRows + tid;
+      // this position's page and scale (layout 0: the page's float32 scales follow its keys)
+      const int32_t pg = pos < ctx ? page_of(pos) : -1;
+      const bool valid = pg >= 0;
+      float sc = 0.f;
+      if (valid)
+        sc = __ldg(reinterpret_cast<const float*>(p.cache + (int64_t)pg * p.P * (kLgDim + 4) + (int64_t)p.P * kLgDim +
+                                                  4 * (pos % p.P)));
+      if (!wait(&bars->tfull[b], (i >> 1) & 1)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      tc_fence_after();
+      float acc = 0.f;
 #pragma unroll
-    for (int c = 0; c < H / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, v);
-      tmem_wait_ld();
+      for (int c = 0; c < H / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + b * H + c * 32, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc = fmaf(sW[c * 32 + i], fmaxf(__uint_as_float(v[i]), 0.f), acc);
+        for (int k = 0; k < 32; ++k) acc = fmaf(sW[c * 32 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[b]);
+      if (pos < p.L) out[pos] = valid ? acc * sc : -INFINITY;
     }
-    if (pos < p.L) out[pos] = my_page >= 0 ? acc * my_scale : -INFINITY;
-  } else if (lane == 0 && p.status != nullptr) {
-    atomicOr(p.status, kStatusTimeout);
+    // positions of this CTA past its last scored tile
+    for (int i = ntiles * kLgRows + tid; i < tpc * kLgRows; i += 128) {
+      const int pos = tile0 * kLgRows + i;
+      if (pos < p.L) out[pos] = -INFINITY;
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, H);
+    tmem_dealloc(tmem, 2 * H);
   }
 }
 
@@ -200,8 +290,8 @@ EncodeTiledFn encode_tiled() {
 
 template <int H>
 cudaError_t launch_logits_h(const LogitsKernelParams& kp, cudaStream_t s) {
-  // at most 512 / H resident CTAs per SM, so that every CTA's TMEM allocation succeeds at once
-  const uint32_t per_sm = 512u / H;
+  // at most 512 / (2H) resident CTAs per SM, so that every CTA's TMEM allocation succeeds at once
+  const uint32_t per_sm = 512u / (2u * H);
   uint32_t smem = lg_smem_used(H) + 1024;
   const uint32_t share = 232448u / per_sm;
   if (smem < share) smem = share;
@@ -214,14 +304,27 @@ cudaError_t launch_logits_h(const LogitsKernelParams& kp, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
-  const dim3 grid((unsigned)((kp.p.L + kLgRows - 1) / kLgRows), (unsigned)kp.p.T);
-  indexer_logits_kernel<H><<<grid, kLgThreads, smem, s>>>(kp);
+  // tiles per CTA: about four waves of resident CTAs over the launch's tiles (counted at the
+  // row length L, since the contexts are device data), 1 .. 8
+  const int tiles_row = (kp.p.L + kLgRows - 1) / kLgRows;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+  const int resident = sms * (int)(232448u / (smem + 1024));
+  int64_t tpc = ((int64_t)tiles_row * kp.p.T) / ((int64_t)(resident > 0 ? resident : 1) * 4);
+  tpc = tpc < 1 ? 1 : (tpc > kLgMaxTilesPerCta ? kLgMaxTilesPerCta : tpc);
+  LogitsKernelParams k2 = kp;
+  k2.tiles_per_cta = (int)tpc;
+  const dim3 grid((unsigned)((tiles_row + tpc - 1) / tpc), (unsigned)kp.p.T);
+  indexer_logits_kernel<H><<<grid, kLgThreads, smem, s>>>(k2);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ top-k
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkVec = 8;                          // consecutive positions per thread in the ordered pass
+constexpr int kTopkChunk = kTopkThreads * kTopkVec;  // positions per ordered-pass step
+constexpr int kTopkSmemKeys = 48 * 1024;             // rows up to this length keep their keys in shared memory
 
 // Order-preserving key of a logit: larger logit, larger key; -inf and NaN map to 0 and are
 // never selected; -0 is read as +0.
@@ -231,32 +334,39 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block-wide ranks of two predicates (in thread order) and their totals.
-__device__ __forceinline__ void block_rank2(bool a, bool b, int& ra, int& rb, int& ta, int& tb, int (*wsum)[2]) {
+// Block-wide exclusive prefix sums of two per-thread counts (thread order) and their totals.
+__device__ __forceinline__ void block_scan2(int a, int b, int& pa, int& pb, int& ta, int& tb, int (*wsum)[2]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t ba = __ballot_sync(0xffffffffu, a), bb = __ballot_sync(0xffffffffu, b);
-  const uint32_t below = (1u << lane) - 1u;
-  if (lane == 0) {
-    wsum[warp][0] = __popc(ba);
-    wsum[warp][1] = __popc(bb);
+  int ia = a, ib = b;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int va = __shfl_up_sync(0xffffffffu, ia, o), vb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += va;
+      ib += vb;
+    }
+  }
+  if (lane == 31) {
+    wsum[warp][0] = ia;
+    wsum[warp][1] = ib;
   }
   __syncthreads();
-  int pa = 0, pb = 0, sa = 0, sb = 0;
+  int wa = 0, wb = 0, sa = 0, sb = 0;
   for (int w = 0; w < kTopkWarps; ++w) {
     const int x = wsum[w][0], y = wsum[w][1];
-    pa += w < warp ? x : 0;
-    pb += w < warp ? y : 0;
+    wa += w < warp ? x : 0;
+    wb += w < warp ? y : 0;
     sa += x;
     sb += y;
   }
-  ra = pa + __popc(ba & below);
-  rb = pb + __popc(bb & below);
+  pa = wa + ia - a;
+  pb = wb + ib - b;
   ta = sa;
   tb = sb;
   __syncthreads();  // wsum is reused by the next call
 }
 
 __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkParams p) {
+  extern __shared__ uint32_t skey[];  // the row's keys when it fits
   __shared__ uint32_t hist[256];
   __shared__ int wsum[kTopkWarps][2];
   __shared__ uint32_t s_bin, s_remaining;
@@ -264,40 +374,80 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
   const int n = max(0, min(__ldg(p.ctx_lens + t), p.L));
   const float* row = p.logits + (int64_t)t * p.stride;
   int32_t* out = p.topk + (int64_t)t * p.K;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool in_smem = p.L <= kTopkSmemKeys;  // the launch gives L keys of shared memory then
+  auto key_at = [&](int i) -> uint32_t { return in_smem ? skey[i] : order_key(__ldg(row + i)); };
 
-  // finite logits
+  // keys into shared memory (one read of the row, four positions per load where aligned)
+  // and the count of finite logits
   int cnt = 0;
-  for (int i = tid; i < n; i += kTopkThreads) cnt += order_key(row[i]) != 0u;
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  if ((tid & 31) == 0) wsum[tid >> 5][0] = cnt;
-  __syncthreads();
-  int total = 0;
-  for (int w = 0; w < kTopkWarps; ++w) total += wsum[w][0];
-  __syncthreads();
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  for (int i0 = tid * 4; i0 < n; i0 += kTopkThreads * 4) {
+    float v[4];
+    if (vec && i0 + 4 <= n) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = i0 + k < n ? __ldg(row + i0 + k) : -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t key = order_key(v[k]);
+      if (in_smem && i0 + k < n) skey[i0 + k] = key;
+      cnt += key != 0u;
+    }
+  }
+  int total;
+  {
+    int pa, pb, tb;
+    block_scan2(cnt, 0, pa, pb, total, tb, wsum);
+  }
 
   uint32_t tau = 0u;      // key of the K-th largest logit (0: take every finite one)
   int need_eq = 0;        // positions equal to tau to take
   if (total > p.K) {
+    const int n_round = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;  // warp-uniform loop bound
     uint32_t prefix = 0u, mask = 0u;
     uint32_t remaining = (uint32_t)p.K;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
       __syncthreads();
-      for (int i = tid; i < n; i += kTopkThreads) {
-        const uint32_t k = order_key(row[i]);
-        if (k != 0u && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+      for (int i = tid; i < n_round; i += kTopkThreads) {
+        const uint32_t k = i < n ? key_at(i) : 0u;
+        const bool take = k != 0u && (k & mask) == prefix;
+        if (__ballot_sync(0xffffffffu, take) == 0u) continue;  // no lane of the warp counts here
+        const uint32_t bin = take ? (k >> shift) & 255u : 256u;
+        // lanes of a warp with the same bin add once, together
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (take && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
       }
       __syncthreads();
-      if (tid == 0) {
-        uint32_t cum = 0u;
-        int b = 255;
-        for (; b > 0; --b) {
-          if (cum + hist[b] >= remaining) break;
-          cum += hist[b];
+      if (tid < 32) {  // the bin holding the remaining-th largest key, from the top
+        // lane l holds bins 255 - 8l .. 248 - 8l; an inclusive scan of the lane sums in lane
+        // order counts the keys in and above each lane's bins
+        uint32_t c[8], sum = 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          c[k] = hist[255 - 8 * lane - k];
+          sum += c[k];
         }
-        s_bin = (uint32_t)b;
-        s_remaining = remaining - cum;
+        uint32_t incl = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const uint32_t above = incl - sum;
+        if (above < remaining && incl >= remaining) {  // exactly one lane
+          uint32_t cum = above;
+          int k = 0;
+          for (; k < 7; ++k) {
+            if (cum + c[k] >= remaining) break;
+            cum += c[k];
+          }
+          s_bin = (uint32_t)(255 - 8 * lane - k);
+          s_remaining = remaining - cum;
+        }
       }
       __syncthreads();
       prefix |= s_bin << shift;
@@ -310,17 +460,30 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
   }
   const int n_gt = total > p.K ? p.K - need_eq : total;  // positions strictly above tau (all finite if none)
   // ordered pass: positions above tau ascending into [0, n_gt), then the lowest positions
-  // equal to tau into [n_gt, K)
+  // equal to tau into [n_gt, K); each thread takes kTopkVec consecutive positions per step
   int base_gt = 0, base_eq = 0;
-  for (int c0 = 0; c0 < n; c0 += kTopkThreads) {
-    const int i = c0 + tid;
-    const uint32_t k = i < n ? order_key(row[i]) : 0u;
-    const bool gt = k != 0u && k > tau;
-    const bool eq = tau != 0u && k == tau;
-    int rg, re, tg, te;
-    block_rank2(gt, eq, rg, re, tg, te, wsum);
-    if (gt) out[base_gt + rg] = i;
-    if (eq && base_eq + re < need_eq) out[n_gt + base_eq + re] = i;
+  for (int c0 = 0; c0 < n; c0 += kTopkChunk) {
+    const int i0 = c0 + tid * kTopkVec;
+    uint32_t keys[kTopkVec];
+    int cg = 0, ce = 0;
+#pragma unroll
+    for (int k = 0; k < kTopkVec; ++k) {
+      keys[k] = i0 + k < n ? key_at(i0 + k) : 0u;
+      cg += keys[k] != 0u && keys[k] > tau;
+      ce += tau != 0u && keys[k] == tau;
+    }
+    int og, oe, tg, te;
+    block_scan2(cg, ce, og, oe, tg, te, wsum);
+    og += base_gt;
+    oe += base_eq;
+#pragma unroll
+    for (int k = 0; k < kTopkVec; ++k) {
+      if (keys[k] != 0u && keys[k] > tau) out[og++] = i0 + k;
+      else if (tau != 0u && keys[k] == tau) {
+        if (oe < need_eq) out[n_gt + oe] = i0 + k;
+        ++oe;
+      }
+    }
     base_gt += tg;
     base_eq += te;
   }
@@ -375,7 +538,20 @@ cudaError_t launch_indexer_logits(const IndexerLogitsParams& p, cudaStream_t s) 
 
 cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
   if (p.T == 0 || p.K == 0) return cudaSuccess;
-  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, 0, s>>>(p);
+  // shared memory for the keys of the longest row that fits (longer rows are read from
+  // global memory on every pass)
+  const int keys = p.L <= kTopkSmemKeys ? p.L : 0;
+  const int smem = keys * 4;
+  static thread_local bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !done[dev]) {
+    e = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemKeys * 4);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) done[dev] = true;
+  }
+  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
