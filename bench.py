@@ -402,6 +402,7 @@ def measure_indexer(api, torch, si, wi, dev, flush, steps: int, peaks: dict, src
                             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": alg,
                             "key_bytes_per_launch": key_bytes,
                             "tensor_tflops_achieved": flops / lg_s / 1e12,
+                            "traffic": load_traffic(wi.name, "indexer_traffic.json", "k_indexer.cu"),
                             "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else "fallback",
                             "kernel": "smd::indexer_logits_kernel"},
         "timing": "events around each launch, L2 flushed before each logits + top-k pair",
@@ -563,16 +564,17 @@ def kernel_code_hash(path: str) -> str:
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
-def load_traffic(name: str):
-    """DRAM bytes per attention launch from a committed ncu summary, if the kernel code is
-    unchanged since the capture."""
-    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
-    src = os.path.join(ROOT, "sparse_mla_decode_req_gb300", "csrc", "k_attn.cu")
+def load_traffic(name: str, profile: str = "attn_traffic.json", source: str = "k_attn.cu"):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, if the kernel's source
+    is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", profile)
+    src = os.path.join(ROOT, "sparse_mla_decode_req_gb300", "csrc", source)
+    key = "k_" + source.split("_", 1)[1].split(".")[0] + "_code_hash"
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(name)
-        if e and e.get("k_attn_code_hash") == kernel_code_hash(src):
+        if e and e.get(key) == kernel_code_hash(src):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass
