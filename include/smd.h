@@ -379,13 +379,14 @@ typedef struct smd_indexer_dims {
  * s < min(ctx_lens[t], L):
  *   logits[t, s] = sum_h weights[t, h] * max(0, sum_d e4m3(q[t, h, d]) * k_s[d])
  * (k_s = the position's key, its bytes times its scale; the rectifier is the reading of
- * the per-head stage, see the design notes).  A position at or past the context, of a
- * block at or past W, of a page outside [0, num_pages) or of a request outside [0, R)
- * gets -inf; every entry of the [T, L] row-major logits array is written.
+ * the per-head stage: a score linear in q would let the heads fold into one vector).  A
+ * position at or past the context, of a block at or past W, of a page outside
+ * [0, num_pages) or of a request outside [0, R) gets -inf; every entry of the [T, L]
+ * row-major logits array is written.
  * q u8 e4m3 [T, H, 128] and cache (layout 0) 16-byte aligned; weights f32 [T, H];
  * logits f32 [T, L] 16-byte aligned; device_status (optional) gets bit 0 if a bounded
  * wait gave up (it is not cleared; zero it before the call).  Tensor cores:
- * tcgen05.mma kind::f8f6f4, one CTA per token and 128 positions.
+ * tcgen05.mma kind::f8f6f4, one CTA per token and 1 to 8 tiles of 128 positions.
  */
 SMD_API int smd_indexer_mqa_logits(const smd_indexer_dims *dims, const uint8_t *q, const float *weights,
                                    const uint8_t *cache, const int32_t *block_table, const int32_t *req_id,

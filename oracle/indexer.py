@@ -23,7 +23,7 @@ What the pages fix, and where:
 * ``topk_positions`` -- the indexer's output is the request-local top-k index list the
   sparse decode reads (``topk_idx`` of ``sparse_mla_decode``).
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
 
 * Cache layout.  The gather kernel takes a LAYOUT switch it does not print.  Layout 0
   (the one the logits use) stores a page of ``P`` positions as ``P * D`` fp8 bytes then

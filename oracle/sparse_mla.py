@@ -24,7 +24,7 @@ Every function is the plain definition of one step, written out in float64:
 * ``lse_combine`` -- log-sum-exp merge of split partials (vLLM PR #52212 report,
   "实现拆解" item 2 and the test symbol ``_launch_sparse_decode_reduce``).
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
 invalid conversion output is -1 (not 0 + ragged lengths); out-of-range request ids
 invalidate the whole token; the sink is an unscaled logit that enters only the
 denominator; ``lse`` is the natural log of the full denominator including the sink;

@@ -11,16 +11,18 @@
 //     64-bit.  One warp per token.
 //
 //   indexer_logits_kernel: the fp8 paged MQA logits (vLLM PR #41217 report, "实现拆解"
-//     item 6: one kernel for the per-head scores and their weighted sum), as read in the
-//     design notes: logit[t, s] = scale_s * sum_h w[t, h] * max(0, q[t, h, :] . k_s) with
-//     e4m3 q and k.  One CTA per (token, 128 positions): TMA brings the tile's key rows
-//     (one 3-D box per page of the 128B-swizzled [page][position][128 bytes] view of
-//     layout 0) and the token's query heads; one elected lane issues four
-//     tcgen05.mma.kind::f8f6f4 (M = 128 positions, N = H heads, K = 32 bytes each) into
-//     TMEM; the four warps read their 32 positions' H head scores back, rectify, weight,
+//     item 6: one kernel for the per-head scores and their weighted sum).  The pages print
+//     no formula; the reading here is logit[t, s] = scale_s * sum_h w[t, h] * max(0,
+//     q[t, h, :] . k_s) with e4m3 q and k (a per-head stage before the sum implies a
+//     per-head non-linearity, taken as the rectifier).  One CTA per token and 1-8 tiles of
+//     128 positions: a TMA warp streams the key rows (one 3-D box per page of the
+//     128B-swizzled [page][position][128 bytes] view of layout 0) through a 4-stage ring
+//     and loads the token's query heads; an MMA warp issues four tcgen05.mma.kind::f8f6f4
+//     per tile (M = 128 positions, N = H heads, K = 32 bytes each) into one of two TMEM
+//     buffers; four warps read their 32 positions' H head scores back, rectify, weight,
 //     sum and scale them.  Positions at or past the token's context, and positions whose
-//     block or page is invalid, get -inf.  The step is bound by reading the key cache
-//     (132 bytes per position against 2 * 128 * H flops on the tensor cores).
+//     request, block or page is invalid, get -inf.  The step is bound by reading the key
+//     cache (132 bytes per position against 2 * 128 * H flops on the tensor cores).
 //
 //   indexer_topk_kernel: per token the K positions of the largest finite logits among its
 //     first ctx_lens[t]: a radix select (four 8-bit passes over order-preserving keys)
