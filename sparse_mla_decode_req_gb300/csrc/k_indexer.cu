@@ -25,11 +25,12 @@
 //     cache (132 bytes per position against 2 * 128 * H flops on the tensor cores).
 //
 //   indexer_topk_kernel: per token the K positions of the largest finite logits among its
-//     first ctx_lens[t]: a radix select (four 8-bit passes over order-preserving keys)
-//     finds the K-th largest logit, then one ordered pass writes the positions above it
-//     (ascending) followed by the lowest positions equal to it; -1 pads a token with
-//     fewer than K finite logits.  One CTA of 1024 threads per token; the logits are read
-//     from L2, six passes.
+//     first ctx_lens[t]: a radix select over order-preserving keys (a 12-bit pass fused
+//     with the one read of the row, then two 10-bit passes over the keys under the chosen
+//     digit) finds the K-th largest logit, then one ordered pass writes the positions
+//     above it (ascending) followed by the lowest positions equal to it; -1 pads a token
+//     with fewer than K finite logits.  One CTA of 512 threads per token, the row's keys
+//     in shared memory when it holds up to 40 K positions.
 #include <cuda.h>
 
 #include "smd_device.cuh"
@@ -326,7 +327,9 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkVec = 8;                          // consecutive positions per thread in the ordered pass
 constexpr int kTopkChunk = kTopkThreads * kTopkVec;  // positions per ordered-pass step
-constexpr int kTopkSmemKeys = 48 * 1024;             // rows up to this length keep their keys in shared memory
+constexpr int kTopkSmemKeys = 40 * 1024;             // rows up to this length keep their keys in shared memory
+constexpr int kTopkCand = 8192;                      // candidates kept after the first radix pass
+constexpr int kTopkBins1 = 4096;                     // first pass: the keys' top 12 bits
 
 // Order-preserving key of a logit: larger logit, larger key; -inf and NaN map to 0 and are
 // never selected; -0 is read as +0.
@@ -367,11 +370,49 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& pa, int& pb, int&
   __syncthreads();  // wsum is reused by the next call
 }
 
+// Counts keys into `hist` by the digit (k >> shift) & (bins - 1) among those with
+// (k & mask) == prefix; lanes of a warp with the same digit add once, together.
+__device__ __forceinline__ void count_digit(uint32_t k, bool in, uint32_t mask, uint32_t prefix, int shift,
+                                            uint32_t bins, uint32_t* hist) {
+  const bool take = in && k != 0u && (k & mask) == prefix;
+  if (__ballot_sync(0xffffffffu, take) == 0u) return;
+  const uint32_t digit = take ? (k >> shift) & (bins - 1u) : bins;
+  const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+  if (take && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+}
+
+// The digit holding the remaining-th largest counted key, scanning `bins` bins from the top,
+// and the rank left inside it.  Every thread of the block calls it.
+__device__ __forceinline__ void pick_digit(const uint32_t* hist, uint32_t bins, uint32_t remaining, int (*wsum)[2],
+                                           uint32_t* s_digit, uint32_t* s_left) {
+  // thread i holds bins (from the top) per*i .. per*i + per - 1
+  const int per = (int)bins / kTopkThreads;  // 8 for 4096 bins, 2 for 1024
+  const int tid = threadIdx.x;
+  int sum = 0;
+  for (int k = 0; k < per; ++k) sum += (int)hist[bins - 1 - (tid * per + k)];
+  int above, pb, total, tb;
+  block_scan2(sum, 0, above, pb, total, tb, wsum);
+  if ((uint32_t)above < remaining && (uint32_t)(above + sum) >= remaining) {  // exactly one thread
+    uint32_t cum = (uint32_t)above;
+    int k = 0;
+    for (; k < per - 1; ++k) {
+      const uint32_t c = hist[bins - 1 - (tid * per + k)];
+      if (cum + c >= remaining) break;
+      cum += c;
+    }
+    *s_digit = bins - 1 - (uint32_t)(tid * per + k);
+    *s_left = remaining - cum;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkParams p) {
-  extern __shared__ uint32_t skey[];  // the row's keys when it fits
-  __shared__ uint32_t hist[256];
+  extern __shared__ uint32_t dyn[];  // [candidates][the row's keys when it fits]
+  __shared__ uint32_t hist[kTopkBins1];
   __shared__ int wsum[kTopkWarps][2];
-  __shared__ uint32_t s_bin, s_remaining;
+  __shared__ uint32_t s_digit, s_left, s_ncand;
+  uint32_t* const cand = dyn;
+  uint32_t* const skey = dyn + kTopkCand;
   const int t = blockIdx.x;
   const int n = max(0, min(__ldg(p.ctx_lens + t), p.L));
   const float* row = p.logits + (int64_t)t * p.stride;
@@ -379,25 +420,39 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
   const int tid = threadIdx.x, lane = tid & 31;
   const bool in_smem = p.L <= kTopkSmemKeys;  // the launch gives L keys of shared memory then
   auto key_at = [&](int i) -> uint32_t { return in_smem ? skey[i] : order_key(__ldg(row + i)); };
+  const int n_round = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;  // warp-uniform loop bound
 
-  // keys into shared memory (one read of the row, four positions per load where aligned)
-  // and the count of finite logits
+  for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist[i] = 0u;
+  if (tid == 0) s_ncand = 0u;
+  __syncthreads();
+  // one read of the row (four vector loads in flight per thread where aligned): keys into
+  // shared memory, the count of finite logits, and the first pass's histogram (top 12 bits)
   int cnt = 0;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  for (int i0 = tid * 4; i0 < n; i0 += kTopkThreads * 4) {
-    float v[4];
-    if (vec && i0 + 4 <= n) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    } else {
+  constexpr int kU = 4;
+  for (int b0 = 0; b0 < n; b0 += kTopkThreads * 4 * kU) {
+    float v[kU][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = i0 + k < n ? __ldg(row + i0 + k) : -INFINITY;
+    for (int u = 0; u < kU; ++u) {
+      const int i0 = b0 + (u * kTopkThreads + tid) * 4;
+      if (vec && i0 + 4 <= n) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
+        v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[u][k] = i0 + k < n ? __ldg(row + i0 + k) : -INFINITY;
+      }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t key = order_key(v[k]);
-      if (in_smem && i0 + k < n) skey[i0 + k] = key;
-      cnt += key != 0u;
+    for (int u = 0; u < kU; ++u) {
+      const int i0 = b0 + (u * kTopkThreads + tid) * 4;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t key = order_key(v[u][k]);
+        if (in_smem && i0 + k < n) skey[i0 + k] = key;
+        cnt += key != 0u;
+        count_digit(key, i0 + k < n, 0u, 0u, 20, kTopkBins1, hist);
+      }
     }
   }
   int total;
@@ -409,52 +464,39 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
   uint32_t tau = 0u;      // key of the K-th largest logit (0: take every finite one)
   int need_eq = 0;        // positions equal to tau to take
   if (total > p.K) {
-    const int n_round = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;  // warp-uniform loop bound
-    uint32_t prefix = 0u, mask = 0u;
-    uint32_t remaining = (uint32_t)p.K;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
+    pick_digit(hist, kTopkBins1, (uint32_t)p.K, wsum, &s_digit, &s_left);
+    uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
+    uint32_t remaining = s_left;
+    // the keys under the chosen 12-bit digit, compacted (unordered) if they fit
+    for (int i = tid; i < n_round; i += kTopkThreads) {
+      const uint32_t k = i < n ? key_at(i) : 0u;
+      const bool c = k != 0u && (k & mask) == prefix;
+      const uint32_t bal = __ballot_sync(0xffffffffu, c);
+      if (bal == 0u) continue;
+      uint32_t base = 0u;
+      if (lane == 0) base = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const uint32_t at = base + __popc(bal & ((1u << lane) - 1u));
+      if (c && at < (uint32_t)kTopkCand) cand[at] = k;
+    }
+    __syncthreads();
+    const uint32_t ncand = s_ncand;
+    const bool compact = ncand <= (uint32_t)kTopkCand;
+    // two more passes of 10 bits, over the candidates (or the whole row if they did not fit)
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
       __syncthreads();
-      for (int i = tid; i < n_round; i += kTopkThreads) {
-        const uint32_t k = i < n ? key_at(i) : 0u;
-        const bool take = k != 0u && (k & mask) == prefix;
-        if (__ballot_sync(0xffffffffu, take) == 0u) continue;  // no lane of the warp counts here
-        const uint32_t bin = take ? (k >> shift) & 255u : 256u;
-        // lanes of a warp with the same bin add once, together
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (take && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+      const int m = compact ? (int)ncand : n;
+      const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+      for (int i = tid; i < m_round; i += kTopkThreads) {
+        const uint32_t k = i < m ? (compact ? cand[i] : key_at(i)) : 0u;
+        count_digit(k, i < m, mask, prefix, shift, 1024u, hist);
       }
       __syncthreads();
-      if (tid < 32) {  // the bin holding the remaining-th largest key, from the top
-        // lane l holds bins 255 - 8l .. 248 - 8l; an inclusive scan of the lane sums in lane
-        // order counts the keys in and above each lane's bins
-        uint32_t c[8], sum = 0u;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          c[k] = hist[255 - 8 * lane - k];
-          sum += c[k];
-        }
-        uint32_t incl = sum;
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const uint32_t above = incl - sum;
-        if (above < remaining && incl >= remaining) {  // exactly one lane
-          uint32_t cum = above;
-          int k = 0;
-          for (; k < 7; ++k) {
-            if (cum + c[k] >= remaining) break;
-            cum += c[k];
-          }
-          s_bin = (uint32_t)(255 - 8 * lane - k);
-          s_remaining = remaining - cum;
-        }
-      }
-      __syncthreads();
-      prefix |= s_bin << shift;
-      mask |= 255u << shift;
-      remaining = s_remaining;
+      pick_digit(hist, 1024u, remaining, wsum, &s_digit, &s_left);
+      prefix |= s_digit << shift;
+      mask |= 1023u << shift;
+      remaining = s_left;
       __syncthreads();
     }
     tau = prefix;
@@ -540,16 +582,17 @@ cudaError_t launch_indexer_logits(const IndexerLogitsParams& p, cudaStream_t s) 
 
 cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
   if (p.T == 0 || p.K == 0) return cudaSuccess;
-  // shared memory for the keys of the longest row that fits (longer rows are read from
-  // global memory on every pass)
+  // shared memory for the candidates and the keys of the longest row that fits (longer rows
+  // are read from global memory on every pass)
   const int keys = p.L <= kTopkSmemKeys ? p.L : 0;
-  const int smem = keys * 4;
+  const int smem = (kTopkCand + keys) * 4;
   static thread_local bool done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !done[dev]) {
-    e = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemKeys * 4);
+    e = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (kTopkCand + kTopkSmemKeys) * 4);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
