@@ -402,7 +402,7 @@ def measure_indexer(api, torch, si, wi, dev, flush, steps: int, peaks: dict, src
                             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": alg,
                             "key_bytes_per_launch": key_bytes,
                             "tensor_tflops_achieved": flops / lg_s / 1e12,
-                            "traffic": load_traffic(wi.name, "indexer_traffic.json", "k_indexer.cu"),
+                            "traffic": load_traffic(wi.name, "indexer_traffic.json", "k_indexer_logits.cu"),
                             "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else "fallback",
                             "kernel": "smd::indexer_logits_kernel"},
         "timing": "events around each launch, L2 flushed before each logits + top-k pair",
