@@ -368,6 +368,30 @@ def measure_indexer(api, torch, si, wi, dev, flush, steps: int, peaks: dict, src
     logits = torch.empty(T, L, dtype=torch.float32, device=dev)
     topk = torch.empty(T, K, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
+    # the key gather of every cached position of every request as one ragged batch
+    lens = torch.tensor(inp.ctx, dtype=torch.int64)
+    cu = torch.zeros(T + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    n_all = int(cu[-1])
+    tts = torch.repeat_interleave(torch.arange(T, dtype=torch.int32), lens).to(dev)
+    cu = cu.to(dev)
+    k_all = torch.empty(n_all, D, dtype=torch.uint8, device=dev)
+    s_all = torch.empty(n_all, dtype=torch.float32, device=dev)
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(3 + steps):
+            flush.zero_()
+            e = gev[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            api.indexer_gather_k(inp.cache, inp.block_table, cu, tts, T, wi.block_size, D, 0, k_out=k_all,
+                                 scale_out=s_all, stream=stream)
+            if e:
+                e[1].record(stream)
+        torch.cuda.synchronize()
+    g_us = [a.elapsed_time(b) * 1e3 for a, b in gev]
+    g_bytes = 2 * n_all * (D + 4) + n_all * 4 * 2  # key bytes and scales read and written, cu/seq ids
+    del k_all, s_all, tts
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     with torch.cuda.stream(stream):
         for i in range(3 + steps):
@@ -405,7 +429,10 @@ def measure_indexer(api, torch, si, wi, dev, flush, steps: int, peaks: dict, src
                             "traffic": load_traffic(wi.name, "indexer_traffic.json", "k_indexer_logits.cu"),
                             "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else "fallback",
                             "kernel": "smd::indexer_logits_kernel"},
-        "timing": "events around each launch, L2 flushed before each logits + top-k pair",
+        "gather_us": {"mean": statistics.mean(g_us), "median": statistics.median(g_us)},
+        "gather_gbs": g_bytes / (statistics.mean(g_us) / 1e6) / 1e9,
+        "gather_frac": g_bytes / (statistics.mean(g_us) / 1e6) / 1e9 / peaks["hbm_gbs"],
+        "timing": "events around each launch, L2 flushed before each logits + top-k pair and each gather",
     }
 
 

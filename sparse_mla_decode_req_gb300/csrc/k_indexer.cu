@@ -28,30 +28,81 @@ namespace {
 // ------------------------------------------------------------------ key gather
 constexpr int kGatherThreads = 256;
 
+// Where token tid's key lives: its page base and in-page position, or nullptr when the
+// token writes nothing (nullptr with `bad_page` when it writes only its zero scale).
+struct GatherSrc {
+  const uint8_t* page;
+  int32_t off;
+  bool bad_page;
+};
+__device__ __forceinline__ GatherSrc gather_src(const IndexerGatherParams& p, int64_t tid) {
+  GatherSrc g{nullptr, 0, false};
+  const int32_t b = __ldg(p.token_to_seq + tid);
+  if (b < 0 || b >= p.B) return g;
+  const int32_t start = __ldg(p.cu_seqlen + b), end = __ldg(p.cu_seqlen + b + 1);
+  if (tid < start || tid >= end) return g;
+  const int64_t pos = tid - start;
+  const int64_t blk = pos / p.P;
+  const int32_t page = blk < p.W ? __ldg(p.block_table + (int64_t)b * p.bt_stride + blk) : -1;
+  if (page < 0 || page >= p.num_pages) {
+    g.bad_page = true;
+    return g;
+  }
+  g.page = p.cache + (int64_t)page * ((int64_t)p.P * (p.D + 4));
+  g.off = (int32_t)(pos - blk * p.P);
+  return g;
+}
+
+// Any layout and head_dim (a multiple of 4): one warp per token, 4-byte words.
 __global__ void __launch_bounds__(kGatherThreads) indexer_gather_kernel(IndexerGatherParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (kGatherThreads / 32);
-  const int64_t page_bytes = (int64_t)p.P * (p.D + 4);
   for (int64_t tid = (int64_t)blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); tid < p.n; tid += warps) {
-    const int32_t b = __ldg(p.token_to_seq + tid);
-    if (b < 0 || b >= p.B) continue;
-    const int32_t start = __ldg(p.cu_seqlen + b), end = __ldg(p.cu_seqlen + b + 1);
-    if (tid < start || tid >= end) continue;
-    const int64_t pos = tid - start;
-    const int64_t blk = pos / p.P;
-    const int32_t off = (int32_t)(pos - blk * p.P);
-    const int32_t page = blk < p.W ? __ldg(p.block_table + (int64_t)b * p.bt_stride + blk) : -1;
-    if (page < 0 || page >= p.num_pages) {
-      if (lane == 0) p.scale_out[tid] = 0.f;
+    const GatherSrc g = gather_src(p, tid);
+    if (g.page == nullptr) {
+      if (g.bad_page && lane == 0) p.scale_out[tid] = 0.f;
       continue;
     }
-    const uint8_t* pg = p.cache + (int64_t)page * page_bytes;
-    const int64_t vo = p.layout == 0 ? (int64_t)off * p.D : (int64_t)off * (p.D + 4);
-    const int64_t so = p.layout == 0 ? (int64_t)p.P * p.D + 4 * off : vo + p.D;
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(pg + vo);
+    const int64_t vo = p.layout == 0 ? (int64_t)g.off * p.D : (int64_t)g.off * (p.D + 4);
+    const int64_t so = p.layout == 0 ? (int64_t)p.P * p.D + 4 * g.off : vo + p.D;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(g.page + vo);
     uint32_t* dst = reinterpret_cast<uint32_t*>(p.k_out + tid * p.D);
     for (int w = lane; w < p.D / 4; w += 32) dst[w] = __ldg(src + w);
-    if (lane == 0) p.scale_out[tid] = __ldg(reinterpret_cast<const float*>(pg + so));
+    if (lane == 0) p.scale_out[tid] = __ldg(reinterpret_cast<const float*>(g.page + so));
+  }
+}
+
+// Layout 0 with 16-byte aligned rows (head_dim a multiple of 16, at most 512): a group of
+// head_dim / 16 lanes per token, one 16-byte load and store each, two tokens per group in
+// flight.
+__global__ void __launch_bounds__(kGatherThreads) indexer_gather16_kernel(IndexerGatherParams p) {
+  const int lanes = p.D >> 4;                 // lanes per token
+  const int groups = 32 / lanes;              // tokens per warp at a time
+  const int lane = threadIdx.x & 31;
+  const int grp = lane / lanes, c = lane - grp * lanes;
+  const bool active = grp < groups;
+  const int64_t per_step = ((int64_t)gridDim.x * (kGatherThreads / 32)) * groups;
+  int64_t tid = ((int64_t)blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5)) * groups + grp;
+  for (; tid < p.n; tid += 2 * per_step) {
+    const int64_t t2 = tid + per_step;
+    const GatherSrc g1 = active ? gather_src(p, tid) : GatherSrc{nullptr, 0, false};
+    const GatherSrc g2 = active && t2 < p.n ? gather_src(p, t2) : GatherSrc{nullptr, 0, false};
+    uint4 v1 = make_uint4(0, 0, 0, 0), v2 = make_uint4(0, 0, 0, 0);
+    float s1 = 0.f, s2 = 0.f;
+    if (g1.page != nullptr) {
+      v1 = ldg_nc_v4(g1.page + (int64_t)g1.off * p.D + 16 * c);
+      if (c == 0) s1 = __ldg(reinterpret_cast<const float*>(g1.page + (int64_t)p.P * p.D + 4 * g1.off));
+    }
+    if (g2.page != nullptr) {
+      v2 = ldg_nc_v4(g2.page + (int64_t)g2.off * p.D + 16 * c);
+      if (c == 0) s2 = __ldg(reinterpret_cast<const float*>(g2.page + (int64_t)p.P * p.D + 4 * g2.off));
+    }
+    if (g1.page != nullptr) *reinterpret_cast<uint4*>(p.k_out + tid * p.D + 16 * c) = v1;
+    if (g2.page != nullptr) *reinterpret_cast<uint4*>(p.k_out + t2 * p.D + 16 * c) = v2;
+    if (c == 0 && active) {
+      if (g1.page != nullptr || g1.bad_page) p.scale_out[tid] = s1;
+      if (t2 < p.n && (g2.page != nullptr || g2.bad_page)) p.scale_out[t2] = s2;
+    }
   }
 }
 
@@ -272,10 +323,16 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
 
 cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s) {
   if (p.n == 0) return cudaSuccess;
-  const int64_t per = kGatherThreads / 32;
+  const bool fast = p.layout == 0 && p.D % 16 == 0 && p.D <= 512 && ((int64_t)p.P * (p.D + 4)) % 16 == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.cache) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.k_out) & 15u) == 0;
+  const int64_t per = (kGatherThreads / 32) * (fast ? 32 / (p.D / 16) * 2 : 1);  // tokens per CTA per step
   int64_t blocks = (p.n + per - 1) / per;
   if (blocks > 65535 * 16) blocks = 65535 * 16;
-  indexer_gather_kernel<<<(unsigned)blocks, kGatherThreads, 0, s>>>(p);
+  if (fast)
+    indexer_gather16_kernel<<<(unsigned)blocks, kGatherThreads, 0, s>>>(p);
+  else
+    indexer_gather_kernel<<<(unsigned)blocks, kGatherThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
