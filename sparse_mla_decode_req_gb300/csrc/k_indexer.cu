@@ -16,7 +16,9 @@
 //     digit) finds the K-th largest logit, then one ordered pass writes the positions
 //     above it (ascending) followed by the lowest positions equal to it; -1 pads a token
 //     with fewer than K finite logits.  One CTA of 512 threads per token, the row's keys
-//     in shared memory when it holds up to 40 K positions.
+//     in shared memory when it holds up to 40 K positions; when the tokens are fewer than
+//     half the SMs, a cluster of four CTAs per token instead (rows up to 64 K positions),
+//     each CTA a quarter of the row, merging their counts through distributed shared memory.
 #include <cuda.h>
 
 #include "smd_device.cuh"
@@ -319,6 +321,193 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
   for (int i = written + tid; i < p.K; i += kTopkThreads) out[i] = -1;
 }
 
+// Four CTAs per token as a cluster, for rows up to 64 K positions: CTA r takes a quarter of
+// the row (its keys and candidates in its own shared memory); the histograms, finite counts
+// and ordered-pass counts are merged by reading the other CTAs' shared memory, so every CTA
+// picks the same digits and writes its own positions at the right offsets.
+constexpr int kTkCluster = 4;
+constexpr int kTkSliceMax = 16 * 1024;   // keys per CTA
+
+__global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(IndexerTopkParams p) {
+  extern __shared__ uint32_t dyn[];        // [slice keys][candidates], kTkSliceMax each at most
+  __shared__ uint32_t hist[kTopkBins1];    // this CTA's counts
+  __shared__ uint32_t mhist[kTopkBins1];   // the cluster's counts
+  __shared__ int wsum[kTopkWarps][2];
+  __shared__ int s_cnt[2];                 // this CTA's published counts
+  __shared__ uint32_t s_digit, s_left, s_ncand;
+  const uint32_t rank = cluster_ctarank();
+  const int t = blockIdx.x / kTkCluster;
+  const int n = max(0, min(__ldg(p.ctx_lens + t), p.L));
+  const int chunk = ((n + kTkCluster - 1) / kTkCluster + 3) & ~3;   // a multiple of 4 positions
+  const int s0 = min(n, (int)rank * chunk), s1 = min(n, s0 + chunk);
+  const int m = s1 - s0;                                             // this CTA's positions
+  const int cap = p.slice_cap;
+  uint32_t* const skey = dyn;
+  uint32_t* const cand = dyn + cap;
+  const float* row = p.logits + (int64_t)t * p.stride + s0;
+  int32_t* out = p.topk + (int64_t)t * p.K;
+  const int tid = threadIdx.x, lane = tid & 31;
+  auto merged = [&](uint32_t* local, int bins) {  // mhist[i] = sum over the cluster of local[i]
+    for (int i = tid; i < bins; i += kTopkThreads) {
+      const uint32_t a = smem_u32(local + i);
+      uint32_t v = 0u;
+#pragma unroll
+      for (int r = 0; r < kTkCluster; ++r) v += ld_cluster_u32(mapa_shared(a, (uint32_t)r));
+      mhist[i] = v;
+    }
+  };
+  auto cluster_sum2 = [&](int a, int b, int& below_a, int& below_b, int& all_a, int& all_b) {
+    // s_cnt published and the cluster synchronised by the caller
+    below_a = below_b = all_a = all_b = 0;
+    for (int r = 0; r < kTkCluster; ++r) {
+      const int x = (int)ld_cluster_u32(mapa_shared(smem_u32(&s_cnt[0]), (uint32_t)r));
+      const int y = (int)ld_cluster_u32(mapa_shared(smem_u32(&s_cnt[1]), (uint32_t)r));
+      if (r < (int)rank) {
+        below_a += x;
+        below_b += y;
+      }
+      all_a += x;
+      all_b += y;
+    }
+    (void)a;
+    (void)b;
+  };
+
+  for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist[i] = 0u;
+  if (tid == 0) s_ncand = 0u;
+  __syncthreads();
+  // one read of the slice: keys into shared memory, the finite count, the 12-bit histogram
+  int cnt = 0;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  constexpr int kU = 4;
+  for (int b0 = 0; b0 < m; b0 += kTopkThreads * 4 * kU) {
+    float v[kU][4];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i0 = b0 + (u * kTopkThreads + tid) * 4;
+      if (vec && i0 + 4 <= m) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
+        v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[u][k] = i0 + k < m ? __ldg(row + i0 + k) : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i0 = b0 + (u * kTopkThreads + tid) * 4;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t key = order_key(v[u][k]);
+        if (i0 + k < m) skey[i0 + k] = key;
+        cnt += key != 0u;
+        count_digit(key, i0 + k < m, 0u, 0u, 20, kTopkBins1, hist);
+      }
+    }
+  }
+  {
+    int pa, pb, tot, tb;
+    block_scan2(cnt, 0, pa, pb, tot, tb, wsum);
+    if (tid == 0) s_cnt[0] = tot;
+  }
+  cluster_sync();
+  int total;
+  {
+    int ba, bb, ab;
+    cluster_sum2(0, 0, ba, bb, total, ab);
+  }
+  merged(hist, kTopkBins1);
+  cluster_sync();  // every CTA has read the others' counts and histograms
+
+  uint32_t tau = 0u;
+  int need_eq = 0;
+  if (total > p.K) {  // the same decision in every CTA of the cluster
+    pick_digit(mhist, kTopkBins1, (uint32_t)p.K, wsum, &s_digit, &s_left);
+    uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
+    uint32_t remaining = s_left;
+    const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+    for (int i = tid; i < m_round; i += kTopkThreads) {
+      const uint32_t k = i < m ? skey[i] : 0u;
+      const bool c = k != 0u && (k & mask) == prefix;
+      const uint32_t bal = __ballot_sync(0xffffffffu, c);
+      if (bal == 0u) continue;
+      uint32_t base = 0u;
+      if (lane == 0) base = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = k;  // candidates <= keys <= cap
+    }
+    __syncthreads();
+    const int nc = (int)s_ncand;
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+      __syncthreads();
+      const int nc_round = (nc + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+      for (int i = tid; i < nc_round; i += kTopkThreads) count_digit(i < nc ? cand[i] : 0u, i < nc, mask, prefix,
+                                                                      shift, 1024u, hist);
+      cluster_sync();
+      merged(hist, 1024);
+      cluster_sync();
+      pick_digit(mhist, 1024u, remaining, wsum, &s_digit, &s_left);
+      prefix |= s_digit << shift;
+      mask |= 1023u << shift;
+      remaining = s_left;
+      __syncthreads();
+    }
+    tau = prefix;
+    need_eq = (int)remaining;
+  }
+  // this CTA's counts above and at tau, then its offsets among the cluster's
+  int lg = 0, le = 0;
+  for (int i = tid; i < m; i += kTopkThreads) {
+    const uint32_t k = skey[i];
+    lg += k != 0u && k > tau;
+    le += tau != 0u && k == tau;
+  }
+  {
+    int pa, pb, ta, tb;
+    block_scan2(lg, le, pa, pb, ta, tb, wsum);
+    if (tid == 0) {
+      s_cnt[0] = ta;
+      s_cnt[1] = tb;
+    }
+  }
+  cluster_sync();
+  int base_gt, base_eq, n_gt, n_eq;
+  cluster_sum2(0, 0, base_gt, base_eq, n_gt, n_eq);
+  cluster_sync();  // the counts are read; the CTAs may now leave once done with their own memory
+  // ordered pass over the slice: positions above tau at [base_gt, ...), the lowest equal ones
+  // at n_gt + [base_eq, ...) while below need_eq
+  for (int c0 = 0; c0 < m; c0 += kTopkChunk) {
+    const int i0 = c0 + tid * kTopkVec;
+    uint32_t keys[kTopkVec];
+    int cg = 0, ce = 0;
+#pragma unroll
+    for (int k = 0; k < kTopkVec; ++k) {
+      keys[k] = i0 + k < m ? skey[i0 + k] : 0u;
+      cg += keys[k] != 0u && keys[k] > tau;
+      ce += tau != 0u && keys[k] == tau;
+    }
+    int og, oe, tg, te;
+    block_scan2(cg, ce, og, oe, tg, te, wsum);
+    og += base_gt;
+    oe += base_eq;
+#pragma unroll
+    for (int k = 0; k < kTopkVec; ++k) {
+      if (keys[k] != 0u && keys[k] > tau) out[og++] = s0 + i0 + k;
+      else if (tau != 0u && keys[k] == tau) {
+        if (oe < need_eq) out[n_gt + oe] = s0 + i0 + k;
+        ++oe;
+      }
+    }
+    base_gt += tg;
+    base_eq += te;
+  }
+  if (rank == 0) {
+    const int written = n_gt + (need_eq < n_eq ? need_eq : n_eq);
+    for (int i = written + tid; i < p.K; i += kTopkThreads) out[i] = -1;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s) {
@@ -338,21 +527,49 @@ cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s) 
 
 cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
   if (p.T == 0 || p.K == 0) return cudaSuccess;
-  // shared memory for the candidates and the keys of the longest row that fits (longer rows
-  // are read from global memory on every pass)
-  const int keys = p.L <= kTopkSmemKeys ? p.L : 0;
-  const int smem = (kTopkCand + keys) * 4;
-  static thread_local bool done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const int slice = ((p.L + kTkCluster - 1) / kTkCluster + 3) & ~3;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+  if (slice <= kTkSliceMax && 2 * p.T <= sms) {
+    // few tokens (one CTA each would leave most SMs idle): a cluster of four CTAs per token,
+    // each with its quarter of the row in shared memory
+    static thread_local bool done_c[64] = {};
+    if (dev < 0 || dev >= 64 || !done_c[dev]) {
+      e = cudaFuncSetAttribute(indexer_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               2 * kTkSliceMax * 4);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) done_c[dev] = true;
+    }
+    IndexerTopkParams q = p;
+    q.slice_cap = slice;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.T * kTkCluster, 1, 1);
+    cfg.blockDim = dim3(kTopkThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)2 * slice * 4;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kTkCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, indexer_topk_cluster_kernel, q);
+  }
+  // many tokens, or rows too long for the clusters: one CTA per token (rows up to 40 K
+  // positions in shared memory, longer ones re-read from global memory on every pass)
+  static thread_local bool done[64] = {};
   if (dev < 0 || dev >= 64 || !done[dev]) {
     e = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (kTopkCand + kTopkSmemKeys) * 4);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
-  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, smem, s>>>(p);
+  const int keys = p.L <= kTopkSmemKeys ? p.L : 0;
+  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, (kTopkCand + keys) * 4, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -530,7 +530,7 @@ SMD_API int smd_indexer_topk(const float* logits, int32_t num_tokens, int32_t ma
   if (k < 1 || k > (1 << 20)) return fail(SMD_ERR_INVALID_ARG, "k %d outside [1, 2^20]", k);
   if (num_tokens == 0) return SMD_OK;
   if (logits == nullptr || ctx_lens == nullptr || topk == nullptr) return fail(SMD_ERR_INVALID_ARG, "NULL pointer");
-  smd::IndexerTopkParams p{logits, ctx_lens, topk, logits_stride, num_tokens, max_len, k};
+  smd::IndexerTopkParams p{logits, ctx_lens, topk, logits_stride, num_tokens, max_len, k, 0};
   const cudaError_t e = smd::launch_indexer_topk(p, stream);
   return e == cudaSuccess ? SMD_OK : cuda_fail(e, "indexer top-k launch");
 }

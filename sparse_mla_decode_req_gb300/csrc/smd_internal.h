@@ -142,6 +142,7 @@ struct IndexerTopkParams {
   int32_t* topk;                 // [T, K]
   int64_t stride;
   int32_t T, L, K;
+  int32_t slice_cap;             // keys per CTA of the clustered kernel (set by the launch)
 };
 cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s);
 

@@ -153,8 +153,12 @@ def _check_topk(got, logits_gpu, ctx, K):
             assert np.all(np.diff(a) > 0)
 
 
-@pytest.mark.parametrize("T,L,K", [(3, 5000, 512), (2, 300, 400), (4, 70000, 2048), (1, 1, 1)])
+@pytest.mark.parametrize("T,L,K", [(3, 5000, 512), (2, 300, 400), (4, 70000, 2048), (1, 1, 1), (80, 3000, 256),
+                                   (96, 45000, 2048)])
 def test_topk_on_synthetic_logits(T, L, K):
+    """Few tokens take the clustered kernel (four CTAs per token), many tokens or rows past
+    64 K positions one CTA per token (keys in shared memory up to 40 K positions, else read
+    from global memory on every pass)."""
     g = torch.Generator(device="cuda").manual_seed(T * L + K)
     lg = torch.randn(T, L, generator=g, device="cuda")
     if L > 100:
