@@ -184,16 +184,30 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
     if (lane == 0) (void)mbar_wait_bounded(&bars->drain, 0, 2000000000ull);
     __syncwarp();
   } else {  // epilogue warps 0-3: warp w owns TMEM lanes (positions) 32w .. 32w+31
-    for (int i = 0; i < ntiles; ++i) {
+    // this thread's position in each of the CTA's tiles: its page and scale (layout 0: the
+    // page's float32 scales follow its keys), all read up front so that their two
+    // dependent round trips are paid once per CTA rather than once per tile
+    int32_t pgs[kLgMaxTilesPerCta];
+    float scs[kLgMaxTilesPerCta];
+#pragma unroll
+    for (int i = 0; i < kLgMaxTilesPerCta; ++i) {
+      const int pos = (tile0 + i) * kLgRows + tid;
+      pgs[i] = i < ntiles && pos < ctx ? page_of(pos) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kLgMaxTilesPerCta; ++i) {
+      const int pos = (tile0 + i) * kLgRows + tid;
+      scs[i] = pgs[i] >= 0 ? __ldg(reinterpret_cast<const float*>(p.cache + (int64_t)pgs[i] * p.P * (kLgDim + 4) +
+                                                                   (int64_t)p.P * kLgDim + 4 * (pos % p.P)))
+                           : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kLgMaxTilesPerCta; ++i) {
+      if (i >= ntiles) break;
       const int b = i & 1;
       const int pos = (tile0 + i) * kLgRows + tid;
-      // this position's page and scale (layout 0: the page's float32 scales follow its keys)
-      const int32_t pg = pos < ctx ? page_of(pos) : -1;
-      const bool valid = pg >= 0;
-      float sc = 0.f;
-      if (valid)
-        sc = __ldg(reinterpret_cast<const float*>(p.cache + (int64_t)pg * p.P * (kLgDim + 4) + (int64_t)p.P * kLgDim +
-                                                  4 * (pos % p.P)));
+      const bool valid = pgs[i] >= 0;
+      const float sc = scs[i];
       if (!wait(&bars->tfull[b], (i >> 1) & 1)) {
         if (lane == 0) give_up();
         break;
@@ -259,13 +273,13 @@ cudaError_t launch_logits_h(const LogitsKernelParams& kp, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
-  // tiles per CTA: about four waves of resident CTAs over the launch's tiles (counted at the
+  // tiles per CTA: about two waves of resident CTAs over the launch's tiles (counted at the
   // row length L, since the contexts are device data), 1 .. 8
   const int tiles_row = (kp.p.L + kLgRows - 1) / kLgRows;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
   const int resident = sms * (int)(232448u / (smem + 1024));
-  int64_t tpc = ((int64_t)tiles_row * kp.p.T) / ((int64_t)(resident > 0 ? resident : 1) * 4);
+  int64_t tpc = ((int64_t)tiles_row * kp.p.T) / ((int64_t)(resident > 0 ? resident : 1) * 2);
   tpc = tpc < 1 ? 1 : (tpc > kLgMaxTilesPerCta ? kLgMaxTilesPerCta : tpc);
   LogitsKernelParams k2 = kp;
   k2.tiles_per_cta = (int)tpc;
