@@ -356,8 +356,9 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
       mhist[i] = v;
     }
   };
-  auto cluster_sum2 = [&](int a, int b, int& below_a, int& below_b, int& all_a, int& all_b) {
-    // s_cnt published and the cluster synchronised by the caller
+  // the two counts every CTA published in s_cnt (after a cluster barrier): the sums over
+  // the CTAs ranked below this one and over all of them
+  auto cluster_sum2 = [&](int& below_a, int& below_b, int& all_a, int& all_b) {
     below_a = below_b = all_a = all_b = 0;
     for (int r = 0; r < kTkCluster; ++r) {
       const int x = (int)ld_cluster_u32(mapa_shared(smem_u32(&s_cnt[0]), (uint32_t)r));
@@ -369,8 +370,6 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
       all_a += x;
       all_b += y;
     }
-    (void)a;
-    (void)b;
   };
 
   for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist[i] = 0u;
@@ -408,13 +407,16 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
   {
     int pa, pb, tot, tb;
     block_scan2(cnt, 0, pa, pb, tot, tb, wsum);
-    if (tid == 0) s_cnt[0] = tot;
+    if (tid == 0) {
+      s_cnt[0] = tot;
+      s_cnt[1] = 0;
+    }
   }
   cluster_sync();
   int total;
   {
     int ba, bb, ab;
-    cluster_sum2(0, 0, ba, bb, total, ab);
+    cluster_sum2(ba, bb, total, ab);
   }
   merged(hist, kTopkBins1);
   cluster_sync();  // every CTA has read the others' counts and histograms
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
   }
   cluster_sync();
   int base_gt, base_eq, n_gt, n_eq;
-  cluster_sum2(0, 0, base_gt, base_eq, n_gt, n_eq);
+  cluster_sum2(base_gt, base_eq, n_gt, n_eq);
   cluster_sync();  // the counts are read; the CTAs may now leave once done with their own memory
   // ordered pass over the slice: positions above tau at [base_gt, ...), the lowest equal ones
   // at n_gt + [base_eq, ...) while below need_eq
