@@ -19,6 +19,7 @@
 //     in shared memory when it holds up to 40 K positions; when the tokens are fewer than
 //     half the SMs, a cluster of four CTAs per token instead (rows up to 64 K positions),
 //     each CTA a quarter of the row, merging their counts through distributed shared memory.
+//     The histograms are shared-memory atomics.
 #include <cuda.h>
 
 #include "smd_device.cuh"
@@ -157,14 +158,12 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& pa, int& pb, int&
 }
 
 // Counts keys into `hist` by the digit (k >> shift) & (bins - 1) among those with
-// (k & mask) == prefix; lanes of a warp with the same digit add once, together.
+// (k & mask) == prefix (shared-memory atomics; aggregating equal digits within a warp with
+// a match instruction first measured slower on GB300: 26.6 against 20.5 µs on the
+// mid-batch indexer shape).
 __device__ __forceinline__ void count_digit(uint32_t k, bool in, uint32_t mask, uint32_t prefix, int shift,
                                             uint32_t bins, uint32_t* hist) {
-  const bool take = in && k != 0u && (k & mask) == prefix;
-  if (__ballot_sync(0xffffffffu, take) == 0u) return;
-  const uint32_t digit = take ? (k >> shift) & (bins - 1u) : bins;
-  const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-  if (take && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+  if (in && k != 0u && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1u)], 1u);
 }
 
 // The digit holding the remaining-th largest counted key, scanning `bins` bins from the top,
