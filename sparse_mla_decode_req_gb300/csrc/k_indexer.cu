@@ -8,7 +8,8 @@
 //     block-table entry whose page must lie in [0, num_pages); the position's D key bytes
 //     go to k_out[tid] and its float32 scale to scale_out[tid] (0, with the key bytes left
 //     as they are, for an invalid page; nothing for an invalid token).  Block offsets are
-//     64-bit.  One warp per token.
+//     64-bit.  Layout 0 with 16-byte aligned rows: a group of head_dim / 16 lanes per
+//     token (indexer_gather16_kernel); otherwise one warp per token in 4-byte words.
 //
 //   indexer_topk_kernel: per token the K positions of the largest finite logits among its
 //     first ctx_lens[t]: a radix select over order-preserving keys (a 12-bit pass fused
