@@ -52,7 +52,7 @@ struct LgBars {
   uint32_t abort;
 };
 
-// One CTA per (token, 8 tiles of 128 positions): a TMA warp streams the key tiles through
+// One CTA per (token, 1-8 tiles of 128 positions): a TMA warp streams the key tiles through
 // a 4-stage ring, an MMA warp scores each tile against the token's H query heads into one
 // of two TMEM buffers (four kind::f8f6f4 UMMAs of K = 32 bytes), and four epilogue warps
 // turn each buffer into 128 logits while the next tile is scored.
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
       __syncwarp();
       ++issued;
     }
-    // every key tile issued has landed before the CTA may leave
+    // every key tile issued has landed before the CTA may leave (2 s bound: work in flight)
     if (lane == 0)
       for (int i = issued - kLgStages < 0 ? 0 : issued - kLgStages; i < issued; ++i)
         (void)mbar_wait_bounded(&bars->full[i % kLgStages], (i / kLgStages) & 1, 2000000000ull);
