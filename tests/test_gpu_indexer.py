@@ -53,6 +53,26 @@ def test_gather_bit_exact(layout, P):
     assert np.array_equal(_np(s).view(np.uint32), rs.view(np.uint32))
 
 
+@pytest.mark.parametrize("D,P", [(48, 64), (512, 16), (36, 64)])
+def test_gather_head_dims(D, P):
+    """Other head sizes: 16-byte lane groups of 3 and 32 lanes (D = 48, 512), and the 4-byte
+    word path (D = 36, rows only 4-byte aligned)."""
+    w = si.small_indexer_workload(num_tokens=4, ctx_lo=30, ctx_hi=150, head_dim=D, block_size=P, extra_pages=1)
+    inp = si.make_indexer_inputs(w, seed=D, device="cuda")
+    lens = inp.ctx
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tts = np.repeat(np.arange(len(lens)), lens).astype(np.int32)
+    n = int(cu[-1])
+    k0 = torch.full((n, D), 0x5A, dtype=torch.uint8, device="cuda")
+    s0 = torch.full((n,), -3.0, dtype=torch.float32, device="cuda")
+    k, s = api.indexer_gather_k(inp.cache, inp.block_table, torch.tensor(cu, device="cuda"),
+                                torch.tensor(tts, device="cuda"), len(lens), P, D, 0, k_out=k0, scale_out=s0)
+    torch.cuda.synchronize()
+    rk, rs = cp_gather_indexer_k(_np(inp.cache), _np(inp.block_table), cu, tts, len(lens), P, D, 0)
+    assert np.array_equal(_np(k), rk)
+    assert np.array_equal(_np(s).view(np.uint32), rs.view(np.uint32))
+
+
 # ----------------------------------------------------------------- logits
 def _abs_bound(inp, max_len):
     """sum_h |w_h| * sum_d |q_hd k_sd| (the magnitude the float32 sums run over)."""
@@ -170,6 +190,24 @@ def test_topk_on_synthetic_logits(T, L, K):
     ctx = torch.tensor([L - 3 * t for t in range(T)], dtype=torch.int32, device="cuda").clamp_min(0)
     got = api.indexer_topk(lg, ctx, K)
     torch.cuda.synchronize()
+    _check_topk(got, lg, _np(ctx), K)
+
+
+@pytest.mark.parametrize("T", [3, 90])
+def test_topk_empty_and_short_rows(T):
+    """Rows of no position, of fewer finite logits than K, and of only -inf, on the
+    clustered (3 tokens) and the single-CTA (90 tokens) kernels."""
+    L, K = 2000, 100
+    lg = torch.randn(T, L, device="cuda")
+    lg[1, :] = -float("inf")
+    ctx = torch.full((T,), L, dtype=torch.int32, device="cuda")
+    ctx[0] = 0
+    ctx[2] = 37
+    got = api.indexer_topk(lg, ctx, K)
+    torch.cuda.synchronize()
+    g = _np(got)
+    assert np.all(g[0] == -1) and np.all(g[1] == -1)
+    assert g[2, :37].tolist() == list(range(37)) and np.all(g[2, 37:] == -1)
     _check_topk(got, lg, _np(ctx), K)
 
 
