@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample length")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16-steps", type=int, default=100,
+                    help="steps of the headline step over a bf16 latent cache; 0 skips it")
     ap.add_argument("--indexer-steps", type=int, default=100,
                     help="steps of the indexer workloads (logits + top-k) measured in the same run; 0 skips them")
     ap.add_argument("--num-splits", type=int, default=None,
@@ -355,6 +357,76 @@ def measure(api, lib, synth, torch, w, seed, dev, flush, K: int, W: int, KP: int
             "comb_ms": [e[2].elapsed_time(e[3]) for e in evk], "out": out, "stream": stream}
 
 
+def measure_bf16_cache(api, torch, synth, w, seed, dev, flush, steps: int, peaks: dict, src: str) -> dict:
+    """The same decode step over a bf16 latent cache (1024-byte rows, no dequantisation):
+    `steps` CUDA-graph replays of the product call (L2 flushed between them) and `steps`
+    attention-only launches over the converted slots, events around each.  Its roofline
+    counts 1024 bytes per valid row; set beside the fp8 step it bounds what dequantising
+    the fp8 rows costs."""
+    inp = synth.make_inputs(w, seed=seed, device=dev)
+    cache = synth.make_cache_bf16(inp.num_pages, w.block_size, seed * 4 + 9, dev)
+    T, H, N = w.num_tokens, w.num_heads, w.n_entries
+    topk = inp.topk_idx if w.topk else None
+    swa = inp.swa_idx if w.swa else None
+    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    dims = api.make_dims(inp.q, cache, inp.block_table, inp.req_id, topk, swa, w.block_size, api.CACHE_BF16)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ws = torch.zeros(api.workspace_size(dims, w.max_splits, sms), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def call():
+        api.sparse_mla_decode(inp.q, cache, inp.block_table, inp.req_id, topk, swa, inp.sink, inp.scale, out=out,
+                              lse=lse, num_splits=w.max_splits, workspace=ws, block_size=w.block_size, stream=stream,
+                              cache_format=api.CACHE_BF16)
+
+    gidx = api.convert_req_index(inp.block_table, inp.req_id, topk, swa, inp.num_pages, w.block_size)
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(3 + steps):
+            flush.zero_()
+            e = ev[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            graph.replay()
+            if e:
+                e[1].record(stream)
+        for i in range(3 + steps):
+            flush.zero_()
+            e = eva[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            api.sparse_mla_attention(inp.q, cache, gidx, inp.sink, inp.scale, num_pages=inp.num_pages,
+                                     num_splits=w.max_splits, block_size=w.block_size, stream=stream,
+                                     cache_format=api.CACHE_BF16)
+            if e:
+                e[1].record(stream)
+        torch.cuda.synchronize()
+    api.read_status(ws)
+    step_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    attn_us = [a.elapsed_time(b) * 1e3 for a, b in eva]
+    rows = inp.n_valid
+    attn_s = statistics.mean(attn_us) / 1e6
+    gbs = rows * 1024.0 / attn_s / 1e9
+    del inp, cache, gidx
+    return {
+        "workload": w.name, "cache_format": "bf16 (1024-byte rows)", "steps": steps,
+        "step_us_median": statistics.median(step_us), "attention_us_mean": statistics.mean(attn_us),
+        "rows_per_s": rows / (statistics.median(step_us) / 1e6),
+        "roofline_attention": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": rows * 1024.0,
+                               "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else "fallback"},
+        "timing": "CUDA-graph replays of smd_sparse_mla_decode and attention-only launches, events around each, "
+                  "512 MiB L2 flush before each",
+    }
+
+
 def measure_indexer(api, torch, si, wi, dev, flush, steps: int, peaks: dict, src: str) -> dict:
     """The indexer step on one of its workloads: `steps` pairs of launches (fp8 paged MQA
     logits, then top-k), L2 flushed before each pair, CUDA events around each launch on the
@@ -525,6 +597,13 @@ def main(argv=None):
             del re_
             torch.cuda.empty_cache()
 
+    # the same headline step over a bf16 latent cache
+    bf16_cache = None
+    if rank == 0 and world == 1 and args.bf16_steps > 0:
+        bf16_cache = measure_bf16_cache(api, torch, synth, w, rank_seed(args.config, 0), dev, flush,
+                                        args.bf16_steps, peaks, src)
+        torch.cuda.empty_cache()
+
     # the indexer step (the top-k source of the decode) on its two workloads
     indexer = {}
     if rank == 0 and world == 1 and args.indexer_steps > 0:
@@ -557,6 +636,7 @@ def main(argv=None):
                               "timing": f"{min(K, 200)} staged steps with events between the kernels "
                                         "(no launch overlap)"},
         "extra_workloads": extras,
+        "bf16_cache": bf16_cache,
         "indexer": indexer,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
