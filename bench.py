@@ -583,6 +583,14 @@ def main(argv=None):
                       "us_per_step": ssecs / e2e["steps"] * 1e6,
                       "method": "one stream: copy in, decode, copy out; each step timed alone after an L2 flush"}
 
+    link_e2e = None
+    if e2e.get("link_seconds") and e2e["steps"] and secs != float("inf"):
+        pair_us = e2e["link_seconds"] / e2e["steps"] * 1e6
+        step_us = secs / e2e["steps"] * 1e6
+        link_e2e = {"copy_pair_us": pair_us, "step_us": step_us, "frac": pair_us / step_us,
+                    "method": "the step's copy in and copy out alone, both directions at once on their "
+                              "two streams, no decode: the host link's bound on the pipelined step"}
+
     # the other target workloads (mid batch, long context; the single-request latency case)
     # measured the same way in the same run, on rank 0's replica only
     extras = {}
@@ -645,6 +653,7 @@ def main(argv=None):
                           "step i's decode), two device buffer sets, three rotating input sets (no L2 reuse "
                           "between consecutive steps); timed from the first copy in to the last copy out",
                 "serial": serial_e2e,
+                "link": link_e2e,
                 "matches_device_path": e2e.get("matches_device_path"), **({"error": e2e["error"]} if "error" in e2e else {})},
         "gpu_launches": K * S_launches,
         "clocks": r["clocks"],
@@ -840,8 +849,26 @@ def run_e2e(api, inp, w, dev, stream, flush, steps, rows_per_step, device_out=No
         step(i)
         torch.cuda.synchronize()
         matches = bool(matches and torch.equal(pack_views(h_res[i & 1], lay_out)["out"], device_out.cpu()))
+
+    # the host link's own bound on this schedule: the same copies in and out, both directions
+    # at once on their two streams, with no decode between them
+    torch.cuda.synchronize()
+    l0, l1, l_in = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                    torch.cuda.Event())
+    l0.record(s_in)
+    s_out.wait_event(l0)
+    for j in range(steps):
+        with torch.cuda.stream(s_in):
+            d_in[j & 1].copy_(h_in[j % len(h_in)], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            h_res[j & 1].copy_(d_res[j & 1], non_blocking=True)
+    l_in.record(s_in)
+    s_out.wait_event(l_in)
+    l1.record(s_out)
+    torch.cuda.synchronize()
+    link_s = l0.elapsed_time(l1) / 1e3
     return {"seconds": pipe_s, "steps": steps, "h2d": nb_in, "d2h": nb_out, "matches_device_path": matches,
-            "serial_seconds": serial_s}
+            "serial_seconds": serial_s, "link_seconds": link_s}
 
 
 if __name__ == "__main__":
