@@ -13,10 +13,10 @@
 //
 //   indexer_topk_kernel: per token the K positions of the largest finite logits among its
 //     first ctx_lens[t]: a radix select over order-preserving keys (a 12-bit pass fused
-//     with the one read of the row, then two 10-bit passes over the keys under the chosen
-//     digit) finds the K-th largest logit, then one ordered pass writes the positions
-//     above it (ascending) followed by the lowest positions equal to it; -1 pads a token
-//     with fewer than K finite logits.  One CTA of 512 threads per token, the row's keys
+//     with the one read of the row; a 10-bit pass that also compacts the keys under the
+//     chosen 12-bit digit; the last 10 bits over those keys alone) finds the K-th largest
+//     logit, then one ordered pass writes the positions above it (ascending) followed by
+//     the lowest positions equal to it; -1 pads a token with fewer than K finite logits.  One CTA of 512 threads per token, the row's keys
 //     in shared memory when it holds up to 40 K positions; when the tokens are fewer than
 //     half the SMs, a cluster of four CTAs per token instead (rows up to 64 K positions),
 //     each CTA a quarter of the row, merging their counts through distributed shared memory.
@@ -113,10 +113,9 @@ __global__ void __launch_bounds__(kGatherThreads) indexer_gather16_kernel(Indexe
 // ------------------------------------------------------------------ top-k
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkVec = 8;                          // consecutive positions per thread in the ordered pass
-constexpr int kTopkChunk = kTopkThreads * kTopkVec;  // positions per ordered-pass step
+constexpr int kTopkChunk = 8192;                     // positions per ordered-pass step (512 per warp)
 constexpr int kTopkSmemKeys = 40 * 1024;             // rows up to this length keep their keys in shared memory
-constexpr int kTopkCand = 8192;                      // candidates kept after the first radix pass
+constexpr int kTopkCand = 8192;                      // candidates kept after the first radix pass (long rows)
 constexpr int kTopkBins1 = 4096;                     // first pass: the keys' top 12 bits
 
 // Order-preserving key of a logit: larger logit, larger key; -inf and NaN map to 0 and are
@@ -143,18 +142,22 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& pa, int& pb, int&
     wsum[warp][1] = ib;
   }
   __syncthreads();
-  int wa = 0, wb = 0, sa = 0, sb = 0;
-  for (int w = 0; w < kTopkWarps; ++w) {
-    const int x = wsum[w][0], y = wsum[w][1];
-    wa += w < warp ? x : 0;
-    wb += w < warp ? y : 0;
-    sa += x;
-    sb += y;
+  // every warp scans the warps' totals with shuffles (lane w holding warp w's)
+  int xa = lane < kTopkWarps ? wsum[lane][0] : 0, xb = lane < kTopkWarps ? wsum[lane][1] : 0;
+#pragma unroll
+  for (int o = 1; o < kTopkWarps; o <<= 1) {
+    const int va = __shfl_up_sync(0xffffffffu, xa, o), vb = __shfl_up_sync(0xffffffffu, xb, o);
+    if (lane >= o) {
+      xa += va;
+      xb += vb;
+    }
   }
-  pa = wa + ia - a;
-  pb = wb + ib - b;
-  ta = sa;
-  tb = sb;
+  const int wa = __shfl_sync(0xffffffffu, xa, warp > 0 ? warp - 1 : 0);
+  const int wb = __shfl_sync(0xffffffffu, xb, warp > 0 ? warp - 1 : 0);
+  pa = (warp > 0 ? wa : 0) + ia - a;
+  pb = (warp > 0 ? wb : 0) + ib - b;
+  ta = __shfl_sync(0xffffffffu, xa, kTopkWarps - 1);
+  tb = __shfl_sync(0xffffffffu, xb, kTopkWarps - 1);
   __syncthreads();  // wsum is reused by the next call
 }
 
@@ -168,9 +171,10 @@ __device__ __forceinline__ void count_digit(uint32_t k, bool in, uint32_t mask, 
 }
 
 // The digit holding the remaining-th largest counted key, scanning `bins` bins from the top,
-// and the rank left inside it.  Every thread of the block calls it.
-__device__ __forceinline__ void pick_digit(const uint32_t* hist, uint32_t bins, uint32_t remaining, int (*wsum)[2],
-                                           uint32_t* s_digit, uint32_t* s_left) {
+// and the rank left inside it (set only when there are at least `remaining` keys); returns
+// the number of keys counted.  Every thread of the block calls it.
+__device__ __forceinline__ int pick_digit(const uint32_t* hist, uint32_t bins, uint32_t remaining, int (*wsum)[2],
+                                          uint32_t* s_digit, uint32_t* s_left) {
   // thread i holds bins (from the top) per*i .. per*i + per - 1
   const int per = (int)bins / kTopkThreads;  // 8 for 4096 bins, 2 for 1024
   const int tid = threadIdx.x;
@@ -190,9 +194,103 @@ __device__ __forceinline__ void pick_digit(const uint32_t* hist, uint32_t bins, 
     *s_left = remaining - cum;
   }
   __syncthreads();
+  return total;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkParams p) {
+// One pass over the keys [0, m) that load4(i, k) gives four at a time (k[j] = the key at
+// i + j, 0 past m): the histogram of the digit (key >> 10) & 1023 of the keys with
+// (key & mask) == prefix into hist (1024 bins, zeroed by the caller), and those keys
+// appended, unordered, to cand while fewer than cap of them (*ncand, zeroed by the caller,
+// ends at their number, which may exceed cap).  A warp makes its appends of a step with one
+// shared-memory atomic, and only in steps where one of its lanes has a key to append.
+// Every thread of the block calls it.
+template <class Load4>
+__device__ __forceinline__ void count_and_compact(Load4 load4, int m, uint32_t mask, uint32_t prefix, uint32_t* hist,
+                                                  uint32_t* cand, uint32_t cap, uint32_t* ncand) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kStep = kTopkThreads * 4;
+  const int m_round = (m + kStep - 1) / kStep * kStep;  // warp-uniform bound
+  for (int i0 = threadIdx.x * 4; i0 < m_round; i0 += kStep) {
+    uint32_t k[4];
+    load4(i0, k);
+    uint32_t hit = 0u;  // bit j: key j is under the prefix
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (k[j] != 0u && (k[j] & mask) == prefix) {
+        hit |= 1u << j;
+        atomicAdd(&hist[(k[j] >> 10) & 1023u], 1u);
+      }
+    }
+    if (__ballot_sync(0xffffffffu, hit != 0u) == 0u) continue;
+    const int c = __popc(hit);
+    int incl = c;  // inclusive scan of the lanes' counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    uint32_t base = 0u;
+    if (lane == 31) base = atomicAdd(ncand, (uint32_t)incl);
+    uint32_t at = __shfl_sync(0xffffffffu, base, 31) + (uint32_t)(incl - c);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((hit >> j) & 1u) {
+        if (at < cap) cand[at] = k[j];
+        ++at;
+      }
+    }
+  }
+}
+
+// Ordered output over the positions [0, m) of a row (or of a CTA's slice of it, position
+// pos0 + i for index i): those whose key is above tau go to out[base_gt + rank] in
+// ascending position, those equal to tau (tau != 0) to out[n_gt + base_eq + rank] while
+// that rank is below need_eq.  Per step each warp owns kTopkChunk / kTopkWarps consecutive
+// positions and lane l takes every 32nd of them from l (shared-memory reads free of bank
+// conflicts); a position's rank is its warp's offset (one block-wide scan of the warps'
+// counts per step) plus the warp ballots of the positions before it.  base_gt and base_eq
+// come back advanced by the counts of [0, m).  Every thread of the block calls it.
+template <class KeyAt>
+__device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, int need_eq, int n_gt, int pos0,
+                                             int32_t* out, int& base_gt, int& base_eq, int (*wsum)[2]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t before = (1u << lane) - 1u;
+  constexpr int kPerWarp = kTopkChunk / kTopkWarps;
+  for (int c0 = 0; c0 < m; c0 += kTopkChunk) {
+    const int w0 = c0 + warp * kPerWarp;
+    constexpr int kSteps = kPerWarp / 32;
+    uint32_t bg[kSteps], be[kSteps];  // the warp's ballots, kept for the writes
+    int cg = 0, ce = 0;               // the warp's counts (warp-uniform)
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k) {
+      const int i = w0 + 32 * k + lane;
+      const uint32_t key = i < m ? key_at(i) : 0u;
+      bg[k] = __ballot_sync(0xffffffffu, key != 0u && key > tau);
+      be[k] = __ballot_sync(0xffffffffu, tau != 0u && key == tau);
+      cg += __popc(bg[k]);
+      ce += __popc(be[k]);
+    }
+    int og, oe, tg, te;
+    block_scan2(lane == 0 ? cg : 0, lane == 0 ? ce : 0, og, oe, tg, te, wsum);
+    og = __shfl_sync(0xffffffffu, og, 0) + base_gt;
+    oe = __shfl_sync(0xffffffffu, oe, 0) + base_eq;
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k) {
+      const int i = w0 + 32 * k + lane;
+      if ((bg[k] >> lane) & 1u) out[og + __popc(bg[k] & before)] = pos0 + i;
+      if ((be[k] >> lane) & 1u) {
+        const int r = oe + __popc(be[k] & before);
+        if (r < need_eq) out[n_gt + r] = pos0 + i;
+      }
+      og += __popc(bg[k]);
+      oe += __popc(be[k]);
+    }
+    base_gt += tg;
+    base_eq += te;
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTopkParams p) {
   extern __shared__ uint32_t dyn[];  // [candidates][the row's keys when it fits]
   __shared__ uint32_t hist[kTopkBins1];
   __shared__ int wsum[kTopkWarps][2];
@@ -203,17 +301,15 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
   const int n = max(0, min(__ldg(p.ctx_lens + t), p.L));
   const float* row = p.logits + (int64_t)t * p.stride;
   int32_t* out = p.topk + (int64_t)t * p.K;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const bool in_smem = p.L <= kTopkSmemKeys;  // the launch gives L keys of shared memory then
   auto key_at = [&](int i) -> uint32_t { return in_smem ? skey[i] : order_key(__ldg(row + i)); };
-  const int n_round = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;  // warp-uniform loop bound
 
   for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist[i] = 0u;
   if (tid == 0) s_ncand = 0u;
   __syncthreads();
   // one read of the row (four vector loads in flight per thread where aligned): keys into
-  // shared memory, the count of finite logits, and the first pass's histogram (top 12 bits)
-  int cnt = 0;
+  // shared memory and the first pass's histogram (top 12 bits) of the finite logits
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
   constexpr int kU = 4;
   for (int b0 = 0; b0 < n; b0 += kTopkThreads * 4 * kU) {
@@ -232,91 +328,75 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int i0 = b0 + (u * kTopkThreads + tid) * 4;
+      uint32_t kk[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t key = order_key(v[u][k]);
-        if (in_smem && i0 + k < n) skey[i0 + k] = key;
-        cnt += key != 0u;
-        count_digit(key, i0 + k < n, 0u, 0u, 20, kTopkBins1, hist);
+        kk[k] = order_key(v[u][k]);
+        count_digit(kk[k], i0 + k < n, 0u, 0u, 20, kTopkBins1, hist);
+      }
+      if (in_smem) {  // one 16-byte store where all four are in the row
+        if (i0 + 4 <= n) *reinterpret_cast<uint4*>(skey + i0) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+        else
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (i0 + k < n) skey[i0 + k] = kk[k];
       }
     }
   }
-  int total;
-  {
-    int pa, pb, tb;
-    block_scan2(cnt, 0, pa, pb, total, tb, wsum);
-  }
+  __syncthreads();
+  // the finite logits' count, and the 12-bit digit holding the K-th largest when above K
+  const int total = pick_digit(hist, kTopkBins1, (uint32_t)p.K, wsum, &s_digit, &s_left);
 
   uint32_t tau = 0u;      // key of the K-th largest logit (0: take every finite one)
   int need_eq = 0;        // positions equal to tau to take
   if (total > p.K) {
-    pick_digit(hist, kTopkBins1, (uint32_t)p.K, wsum, &s_digit, &s_left);
     uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
     uint32_t remaining = s_left;
-    // the keys under the chosen 12-bit digit, compacted (unordered) if they fit
-    for (int i = tid; i < n_round; i += kTopkThreads) {
-      const uint32_t k = i < n ? key_at(i) : 0u;
-      const bool c = k != 0u && (k & mask) == prefix;
-      const uint32_t bal = __ballot_sync(0xffffffffu, c);
-      if (bal == 0u) continue;
-      uint32_t base = 0u;
-      if (lane == 0) base = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      const uint32_t at = base + __popc(bal & ((1u << lane) - 1u));
-      if (c && at < (uint32_t)kTopkCand) cand[at] = k;
-    }
+    // the next 10 bits: one pass over the row counts them for the keys under the chosen
+    // 12-bit digit and compacts those keys (unordered) while they fit
+    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+    __syncthreads();
+    const bool vec_row = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    count_and_compact(
+        [&](int i0, uint32_t (&k)[4]) {
+          if (in_smem && i0 + 4 <= n) {
+            const uint4 v = *reinterpret_cast<const uint4*>(skey + i0);
+            k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+          } else if (!in_smem && vec_row && i0 + 4 <= n) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
+            k[0] = order_key(f.x); k[1] = order_key(f.y); k[2] = order_key(f.z); k[3] = order_key(f.w);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) k[j] = i0 + j < n ? key_at(i0 + j) : 0u;
+          }
+        },
+        n, mask, prefix, hist, cand, (uint32_t)kTopkCand, &s_ncand);
     __syncthreads();
     const uint32_t ncand = s_ncand;
+    (void)pick_digit(hist, 1024u, remaining, wsum, &s_digit, &s_left);
+    prefix |= s_digit << 10;
+    mask |= 1023u << 10;
+    remaining = s_left;
+    // the last 10 bits over the candidates (or the whole row if they did not fit)
+    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+    __syncthreads();
     const bool compact = ncand <= (uint32_t)kTopkCand;
-    // two more passes of 10 bits, over the candidates (or the whole row if they did not fit)
-    for (int shift = 10; shift >= 0; shift -= 10) {
-      for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
-      __syncthreads();
-      const int m = compact ? (int)ncand : n;
-      const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-      for (int i = tid; i < m_round; i += kTopkThreads) {
-        const uint32_t k = i < m ? (compact ? cand[i] : key_at(i)) : 0u;
-        count_digit(k, i < m, mask, prefix, shift, 1024u, hist);
-      }
-      __syncthreads();
-      pick_digit(hist, 1024u, remaining, wsum, &s_digit, &s_left);
-      prefix |= s_digit << shift;
-      mask |= 1023u << shift;
-      remaining = s_left;
-      __syncthreads();
+    const int m = compact ? (int)ncand : n;
+    const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+    for (int i = tid; i < m_round; i += kTopkThreads) {
+      const uint32_t k = i < m ? (compact ? cand[i] : key_at(i)) : 0u;
+      count_digit(k, i < m, mask, prefix, 0, 1024u, hist);
     }
-    tau = prefix;
-    need_eq = (int)remaining;
+    __syncthreads();
+    (void)pick_digit(hist, 1024u, remaining, wsum, &s_digit, &s_left);
+    tau = prefix | s_digit;
+    need_eq = (int)s_left;
   }
   const int n_gt = total > p.K ? p.K - need_eq : total;  // positions strictly above tau (all finite if none)
   // ordered pass: positions above tau ascending into [0, n_gt), then the lowest positions
-  // equal to tau into [n_gt, K); each thread takes kTopkVec consecutive positions per step
+  // equal to tau into [n_gt, K)
   int base_gt = 0, base_eq = 0;
-  for (int c0 = 0; c0 < n; c0 += kTopkChunk) {
-    const int i0 = c0 + tid * kTopkVec;
-    uint32_t keys[kTopkVec];
-    int cg = 0, ce = 0;
-#pragma unroll
-    for (int k = 0; k < kTopkVec; ++k) {
-      keys[k] = i0 + k < n ? key_at(i0 + k) : 0u;
-      cg += keys[k] != 0u && keys[k] > tau;
-      ce += tau != 0u && keys[k] == tau;
-    }
-    int og, oe, tg, te;
-    block_scan2(cg, ce, og, oe, tg, te, wsum);
-    og += base_gt;
-    oe += base_eq;
-#pragma unroll
-    for (int k = 0; k < kTopkVec; ++k) {
-      if (keys[k] != 0u && keys[k] > tau) out[og++] = i0 + k;
-      else if (tau != 0u && keys[k] == tau) {
-        if (oe < need_eq) out[n_gt + oe] = i0 + k;
-        ++oe;
-      }
-    }
-    base_gt += tg;
-    base_eq += te;
-  }
+  ordered_pass(key_at, n, tau, need_eq, n_gt, 0, out, base_gt, base_eq, wsum);
   const int written = n_gt + (need_eq < base_eq ? need_eq : base_eq);
   for (int i = written + tid; i < p.K; i += kTopkThreads) out[i] = -1;
 }
@@ -328,7 +408,7 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_kernel(IndexerTopkP
 constexpr int kTkCluster = 4;
 constexpr int kTkSliceMax = 16 * 1024;   // keys per CTA
 
-__global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(IndexerTopkParams p) {
+__global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(IndexerTopkParams p) {
   extern __shared__ uint32_t dyn[];        // [slice keys][candidates], kTkSliceMax each at most
   __shared__ uint32_t hist[kTopkBins1];    // this CTA's counts
   __shared__ uint32_t mhist[kTopkBins1];   // the cluster's counts
@@ -346,7 +426,7 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
   uint32_t* const cand = dyn + cap;
   const float* row = p.logits + (int64_t)t * p.stride + s0;
   int32_t* out = p.topk + (int64_t)t * p.K;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   auto merged = [&](uint32_t* local, int bins) {  // mhist[i] = sum over the cluster of local[i]
     for (int i = tid; i < bins; i += kTopkThreads) {
       const uint32_t a = smem_u32(local + i);
@@ -373,10 +453,8 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
   };
 
   for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist[i] = 0u;
-  if (tid == 0) s_ncand = 0u;
   __syncthreads();
-  // one read of the slice: keys into shared memory, the finite count, the 12-bit histogram
-  int cnt = 0;
+  // one read of the slice: keys into shared memory and the 12-bit histogram of the finite logits
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
   constexpr int kU = 4;
   for (int b0 = 0; b0 < m; b0 += kTopkThreads * 4 * kU) {
@@ -395,61 +473,60 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int i0 = b0 + (u * kTopkThreads + tid) * 4;
+      uint32_t kk[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t key = order_key(v[u][k]);
-        if (i0 + k < m) skey[i0 + k] = key;
-        cnt += key != 0u;
-        count_digit(key, i0 + k < m, 0u, 0u, 20, kTopkBins1, hist);
+        kk[k] = order_key(v[u][k]);
+        count_digit(kk[k], i0 + k < m, 0u, 0u, 20, kTopkBins1, hist);
       }
+      if (i0 + 4 <= m) *reinterpret_cast<uint4*>(skey + i0) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+      else
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (i0 + k < m) skey[i0 + k] = kk[k];
     }
   }
-  {
-    int pa, pb, tot, tb;
-    block_scan2(cnt, 0, pa, pb, tot, tb, wsum);
-    if (tid == 0) {
-      s_cnt[0] = tot;
-      s_cnt[1] = 0;
-    }
-  }
-  cluster_sync();
-  int total;
-  {
-    int ba, bb, ab;
-    cluster_sum2(ba, bb, total, ab);
-  }
+  cluster_sync();  // every CTA's histogram complete
   merged(hist, kTopkBins1);
-  cluster_sync();  // every CTA has read the others' counts and histograms
+  cluster_sync();  // every CTA has read the others' histograms
+  // the cluster's finite count, and the 12-bit digit holding the K-th largest when above K
+  const int total = pick_digit(mhist, kTopkBins1, (uint32_t)p.K, wsum, &s_digit, &s_left);
 
   uint32_t tau = 0u;
   int need_eq = 0;
   if (total > p.K) {  // the same decision in every CTA of the cluster
-    pick_digit(mhist, kTopkBins1, (uint32_t)p.K, wsum, &s_digit, &s_left);
     uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
     uint32_t remaining = s_left;
-    const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-    for (int i = tid; i < m_round; i += kTopkThreads) {
-      const uint32_t k = i < m ? skey[i] : 0u;
-      const bool c = k != 0u && (k & mask) == prefix;
-      const uint32_t bal = __ballot_sync(0xffffffffu, c);
-      if (bal == 0u) continue;
-      uint32_t base = 0u;
-      if (lane == 0) base = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = k;  // candidates <= keys <= cap
-    }
+    // the next 10 bits: one pass over the slice counts them for the keys under the chosen
+    // 12-bit digit and compacts those keys; the last 10 bits are counted over those alone
+    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+    if (tid == 0) s_ncand = 0u;
     __syncthreads();
-    const int nc = (int)s_ncand;
+    count_and_compact(
+        [&](int i0, uint32_t (&k)[4]) {
+          if (i0 + 4 <= m) {
+            const uint4 v = *reinterpret_cast<const uint4*>(skey + i0);
+            k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) k[j] = i0 + j < m ? skey[i0 + j] : 0u;
+          }
+        },
+        m, mask, prefix, hist, cand, (uint32_t)cap, &s_ncand);
+    __syncthreads();
+    const int nc = (int)s_ncand;  // <= m <= cap
+    const int nc_round = (nc + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
     for (int shift = 10; shift >= 0; shift -= 10) {
-      for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
-      __syncthreads();
-      const int nc_round = (nc + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-      for (int i = tid; i < nc_round; i += kTopkThreads) count_digit(i < nc ? cand[i] : 0u, i < nc, mask, prefix,
-                                                                      shift, 1024u, hist);
+      if (shift == 0) {
+        for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < nc_round; i += kTopkThreads)
+          count_digit(i < nc ? cand[i] : 0u, i < nc, mask, prefix, 0, 1024u, hist);
+      }
       cluster_sync();
       merged(hist, 1024);
       cluster_sync();
-      pick_digit(mhist, 1024u, remaining, wsum, &s_digit, &s_left);
+      (void)pick_digit(mhist, 1024u, remaining, wsum, &s_digit, &s_left);
       prefix |= s_digit << shift;
       mask |= 1023u << shift;
       remaining = s_left;
@@ -479,31 +556,7 @@ __global__ void __launch_bounds__(kTopkThreads) indexer_topk_cluster_kernel(Inde
   cluster_sync();  // the counts are read; the CTAs may now leave once done with their own memory
   // ordered pass over the slice: positions above tau at [base_gt, ...), the lowest equal ones
   // at n_gt + [base_eq, ...) while below need_eq
-  for (int c0 = 0; c0 < m; c0 += kTopkChunk) {
-    const int i0 = c0 + tid * kTopkVec;
-    uint32_t keys[kTopkVec];
-    int cg = 0, ce = 0;
-#pragma unroll
-    for (int k = 0; k < kTopkVec; ++k) {
-      keys[k] = i0 + k < m ? skey[i0 + k] : 0u;
-      cg += keys[k] != 0u && keys[k] > tau;
-      ce += tau != 0u && keys[k] == tau;
-    }
-    int og, oe, tg, te;
-    block_scan2(cg, ce, og, oe, tg, te, wsum);
-    og += base_gt;
-    oe += base_eq;
-#pragma unroll
-    for (int k = 0; k < kTopkVec; ++k) {
-      if (keys[k] != 0u && keys[k] > tau) out[og++] = s0 + i0 + k;
-      else if (tau != 0u && keys[k] == tau) {
-        if (oe < need_eq) out[n_gt + oe] = s0 + i0 + k;
-        ++oe;
-      }
-    }
-    base_gt += tg;
-    base_eq += te;
-  }
+  ordered_pass([&](int i) { return skey[i]; }, m, tau, need_eq, n_gt, s0, out, base_gt, base_eq, wsum);
   if (rank == 0) {
     const int written = n_gt + (need_eq < n_eq ? need_eq : n_eq);
     for (int i = written + tid; i < p.K; i += kTopkThreads) out[i] = -1;
@@ -571,7 +624,7 @@ cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
   const int keys = p.L <= kTopkSmemKeys ? p.L : 0;
-  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, (kTopkCand + keys) * 4, s>>>(p);
+  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, (size_t)(kTopkCand + keys) * 4, s>>>(p);
   return cudaGetLastError();
 }
 
