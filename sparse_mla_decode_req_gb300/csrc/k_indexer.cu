@@ -8,7 +8,8 @@
 //     block-table entry whose page must lie in [0, num_pages); the position's D key bytes
 //     go to k_out[tid] and its float32 scale to scale_out[tid] (0, with the key bytes left
 //     as they are, for an invalid page; nothing for an invalid token).  Block offsets are
-//     64-bit.  Layout 0 with 16-byte aligned rows: a group of head_dim / 16 lanes per
+//     64-bit.  Layout 0 with 16-byte aligned rows: 32 tokens per warp when head_dim / 16 is
+//     a power of two (indexer_gather_warp_kernel), else a group of head_dim / 16 lanes per
 //     token (indexer_gather16_kernel); otherwise one warp per token in 4-byte words.
 //
 //   indexer_topk_kernel: per token the K positions of the largest finite logits among its
@@ -107,6 +108,53 @@ __global__ void __launch_bounds__(kGatherThreads) indexer_gather16_kernel(Indexe
       if (g1.page != nullptr || g1.bad_page) p.scale_out[tid] = s1;
       if (t2 < p.n && (g2.page != nullptr || g2.bad_page)) p.scale_out[t2] = s2;
     }
+  }
+}
+
+// Layout 0 with 16-byte aligned rows and PIECES = head_dim / 16 a power of two (head_dim
+// 16 .. 512): each warp takes 32 consecutive tokens per step.  Lane l resolves token l's
+// page and in-page position (the index reads coalesced across the warp) and moves its
+// scale; then the warp copies the 32 rows as 32 * PIECES 16-byte pieces, lane l taking
+// pieces l, l + 32, ... (consecutive lanes on consecutive bytes of consecutive rows), up to
+// eight of them in flight per lane, each piece's row pointer passed by a shuffle from the
+// lane that resolved it.  Four CTAs per SM (64 registers a thread): the bytes in flight,
+// not the instructions, set its rate (three CTAs at 78 registers moved 0.80 of the measured
+// copy bandwidth on the large-batch indexer shape, four 0.89, six, spilling, 0.77).
+template <int PIECES>
+__global__ void __launch_bounds__(kGatherThreads, 4) indexer_gather_warp_kernel(IndexerGatherParams p) {
+  static_assert(PIECES >= 1 && PIECES <= 32 && (PIECES & (PIECES - 1)) == 0, "a power of two up to 32");
+  constexpr int kRound = PIECES < 8 ? PIECES : 8;  // pieces per lane in flight
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (kGatherThreads / 32);
+  for (int64_t t0 = ((int64_t)blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5)) * 32; t0 < p.n;
+       t0 += nwarps * 32) {
+    const int64_t tid = t0 + lane;
+    const GatherSrc g = tid < p.n ? gather_src(p, tid) : GatherSrc{nullptr, 0, false};
+    const uint8_t* row = g.page != nullptr ? g.page + (int64_t)g.off * p.D : nullptr;
+    float sc = 0.f;
+    if (g.page != nullptr) sc = __ldg(reinterpret_cast<const float*>(g.page + (int64_t)p.P * p.D + 4 * g.off));
+    const unsigned long long rp = reinterpret_cast<unsigned long long>(row);
+#pragma unroll 1
+    for (int j0 = 0; j0 < PIECES; j0 += kRound) {
+      uint4 v[kRound];
+      uint32_t have = 0u;  // bit j: piece j's row is valid
+#pragma unroll
+      for (int j = 0; j < kRound; ++j) {
+        const int q = lane + 32 * (j0 + j);  // piece q: row q / PIECES, piece q % PIECES of it
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, rp, q / PIECES));
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (src != nullptr) {
+          v[j] = ldg_nc_v4(src + 16 * (q % PIECES));
+          have |= 1u << j;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kRound; ++j) {
+        const int q = lane + 32 * (j0 + j);
+        if ((have >> j) & 1u) *reinterpret_cast<uint4*>(p.k_out + (t0 + q / PIECES) * p.D + 16 * (q % PIECES)) = v[j];
+      }
+    }
+    if (tid < p.n && (g.page != nullptr || g.bad_page)) p.scale_out[tid] = sc;
   }
 }
 
@@ -570,6 +618,20 @@ cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s) 
   const bool fast = p.layout == 0 && p.D % 16 == 0 && p.D <= 512 && ((int64_t)p.P * (p.D + 4)) % 16 == 0 &&
                     (reinterpret_cast<uintptr_t>(p.cache) & 15u) == 0 &&
                     (reinterpret_cast<uintptr_t>(p.k_out) & 15u) == 0;
+  const int pieces = p.D / 16;
+  if (fast && (pieces & (pieces - 1)) == 0) {  // 32 tokens per warp
+    int64_t blocks = (p.n + (kGatherThreads / 32) * 32 - 1) / ((kGatherThreads / 32) * 32);
+    if (blocks > 65535 * 16) blocks = 65535 * 16;
+    switch (pieces) {
+      case 1: indexer_gather_warp_kernel<1><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+      case 2: indexer_gather_warp_kernel<2><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+      case 4: indexer_gather_warp_kernel<4><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+      case 8: indexer_gather_warp_kernel<8><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+      case 16: indexer_gather_warp_kernel<16><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+      default: indexer_gather_warp_kernel<32><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+    }
+    return cudaGetLastError();
+  }
   const int64_t per = (kGatherThreads / 32) * (fast ? 32 / (p.D / 16) * 2 : 1);  // tokens per CTA per step
   int64_t blocks = (p.n + per - 1) / per;
   if (blocks > 65535 * 16) blocks = 65535 * 16;
