@@ -53,10 +53,11 @@ def test_gather_bit_exact(layout, P):
     assert np.array_equal(_np(s).view(np.uint32), rs.view(np.uint32))
 
 
-@pytest.mark.parametrize("D,P", [(48, 64), (512, 16), (36, 64)])
+@pytest.mark.parametrize("D,P", [(48, 64), (512, 16), (36, 64), (16, 64), (32, 64), (64, 16), (256, 64)])
 def test_gather_head_dims(D, P):
-    """Other head sizes: 16-byte lane groups of 3 and 32 lanes (D = 48, 512), and the 4-byte
-    word path (D = 36, rows only 4-byte aligned)."""
+    """Other head sizes: 32 tokens per warp with 1, 2, 4, 16 and 32 16-byte pieces per row
+    (D = 16, 32, 64, 256, 512), a 16-byte lane group of 3 (D = 48), and the 4-byte word
+    path (D = 36, rows only 4-byte aligned)."""
     w = si.small_indexer_workload(num_tokens=4, ctx_lo=30, ctx_hi=150, head_dim=D, block_size=P, extra_pages=1)
     inp = si.make_indexer_inputs(w, seed=D, device="cuda")
     lens = inp.ctx
