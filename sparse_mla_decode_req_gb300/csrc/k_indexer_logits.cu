@@ -5,8 +5,9 @@
 //     no formula; the reading here is logit[t, s] = scale_s * sum_h w[t, h] * max(0,
 //     q[t, h, :] . k_s) with e4m3 q and k (a per-head stage before the sum implies a
 //     per-head non-linearity, taken as the rectifier).  One CTA per token and 1-8 tiles of
-//     128 positions: a TMA warp streams the key rows (one 3-D box per page of the
-//     128B-swizzled [page][position][128 bytes] view of layout 0) through a 4-stage ring
+//     128 positions: a TMA warp reads the pages of all its tiles at once (its lanes, one
+//     round trip) and streams the key rows (one 3-D box per page of the 128B-swizzled
+//     [page][position][128 bytes] view of layout 0) through a 4-stage ring
 //     and loads the token's query heads; an MMA warp issues four tcgen05.mma.kind::f8f6f4
 //     per tile (M = 128 positions, N = H heads, K = 32 bytes each) into one of two TMEM
 //     buffers; four warps read their 32 positions' H head scores back, rectify, weight,
@@ -30,8 +31,9 @@ constexpr int kLgThreads = 192;     // warps 0-3 epilogue (one TMEM lane quarter
 constexpr int kLgTmaWarp = 4, kLgMmaWarp = 5;
 constexpr uint32_t kLgKBytes = kLgRows * kLgDim;  // 16 KB key tile
 
+constexpr int kLgMaxPages = kLgMaxTilesPerCta * kLgRows / 8;  // pages a CTA's tiles span, at most (P >= 8)
 __host__ __device__ constexpr uint32_t lg_smem_used(int H) {
-  return kLgStages * kLgKBytes + (uint32_t)H * kLgDim + (uint32_t)H * 4 + 256;
+  return kLgStages * kLgKBytes + (uint32_t)H * kLgDim + (uint32_t)H * 4 + 256 + kLgMaxPages * 4;
 }
 
 struct LogitsKernelParams {
@@ -51,6 +53,7 @@ struct LgBars {
   uint32_t tmem;
   uint32_t abort;
 };
+static_assert(sizeof(LgBars) <= 256, "the barriers fit the 256 bytes before the page list");
 
 // One CTA per (token, 1-8 tiles of 128 positions): a TMA warp streams the key tiles through
 // a 4-stage ring, an MMA warp scores each tile against the token's H query heads into one
@@ -79,6 +82,7 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
   uint8_t* const sQ = smem + kLgStages * kLgKBytes;           // [H heads][128 B] (1 KB aligned)
   float* const sW = reinterpret_cast<float*>(sQ + H * kLgDim);
   LgBars* const bars = reinterpret_cast<LgBars*>(sW + H);
+  int32_t* const sPage = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + 256);  // the TMA warp's page list
   const uint64_t limit = p.wait_limit_ns;
 
   const int32_t r = __ldg(p.req_id + t);
@@ -138,6 +142,11 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
       mbar_arrive_expect_tx(&bars->qfull, H * kLgDim);
       tma_load_2d(smem_u32(sQ), &kp.qmap, 0, t * H, &bars->qfull);
     }
+    // the pages of all the CTA's tiles, read by the warp's lanes at once (one round trip)
+    // rather than by the issuing lane box by box
+    const int ppt = kLgRows / p.P;  // pages per tile (P divides 128)
+    for (int g = lane; g < ntiles * ppt; g += 32) sPage[g] = page_of(tile0 * kLgRows + g * p.P);
+    __syncwarp();
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % kLgStages;
       if (i >= kLgStages && !wait(&bars->empty[s], ((i / kLgStages) - 1) & 1)) {
@@ -145,11 +154,10 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
         break;
       }
       if (lane == 0) {
-        const int pos0 = (tile0 + i) * kLgRows;
         mbar_arrive_expect_tx(&bars->full[s], kLgKBytes);
         // one box per page of the tile (P divides 128); an invalid page reads as zeros
-        for (int j = 0; j < kLgRows / p.P; ++j)
-          tma_load_3d(smem_u32(sK + s * kLgKBytes) + j * p.P * kLgDim, &kp.kmap, 0, 0, page_of(pos0 + j * p.P),
+        for (int j = 0; j < ppt; ++j)
+          tma_load_3d(smem_u32(sK + s * kLgKBytes) + j * p.P * kLgDim, &kp.kmap, 0, 0, sPage[i * ppt + j],
                       &bars->full[s]);
       }
       __syncwarp();
