@@ -149,6 +149,30 @@ def test_logits_full_size_sampled():
     _check_logits(got, inp, L, toks)
 
 
+def test_gather_full_size_prefix():
+    """The key gather of every cached position of the large-batch indexer shape (256
+    sequences of 8192 positions, 2 097 152 tokens) in the launch the benchmark times; the
+    first three sequences' 24 576 tokens against the oracle bit for bit, and no row past
+    the batch touched."""
+    w = si.INDEXER_WORKLOADS[1]
+    inp = si.make_indexer_inputs(w, device="cuda")
+    lens = np.asarray(inp.ctx)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    n = int(cu[-1])
+    tts = np.repeat(np.arange(len(lens)), lens).astype(np.int32)
+    D, P = w.head_dim, w.block_size
+    k0 = torch.full((n + 64, D), 0x3C, dtype=torch.uint8, device="cuda")
+    s0 = torch.full((n + 64,), 9.0, dtype=torch.float32, device="cuda")
+    api.indexer_gather_k(inp.cache, inp.block_table, torch.tensor(cu, device="cuda"), torch.tensor(tts, device="cuda"),
+                         len(lens), P, D, 0, k_out=k0[:n], scale_out=s0[:n])
+    torch.cuda.synchronize()
+    m = int(cu[3])
+    rk, rs = cp_gather_indexer_k(_np(inp.cache), _np(inp.block_table), cu[:4], tts[:m], 3, P, D, 0)
+    assert np.array_equal(_np(k0[:m]), rk)
+    assert np.array_equal(_np(s0[:m]).view(np.uint32), rs.view(np.uint32))
+    assert bool((k0[n:] == 0x3C).all()) and bool((s0[n:] == 9.0).all())
+
+
 # ----------------------------------------------------------------- top-k
 def _check_topk(got, logits_gpu, ctx, K):
     lg = _np(logits_gpu).astype(np.float64)
