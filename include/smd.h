@@ -145,13 +145,14 @@ typedef struct smd_decode_opts {
  * split-K parts S the decode will use, or a negative status.  num_splits: 0 = automatic
  * with cap 32; n > 0 = automatic with cap n; n < 0 = exactly -n (1..32).  The automatic
  * choice depends only on the shapes and num_sms, so a captured CUDA graph stays valid:
- * the S in 1..cap (cap at most 4 for "short" steps, K+W <= 1024 entries) that minimises
- * waves x (tiles per split + 4) + (S > 1 ? 2 : 0), with 64-row tiles, waves =
- * ceil(T x S x ceil(H / 64) / num_sms) (one CTA per token, split and group of 64 heads,
- * one CTA per SM) and 4 and 2 the fixed cost of a work item and of the combine in tiles;
- * every split keeps >= 1 tile (vLLM PR #52212 report, "实现拆解" item 2: occupancy
- * target, short work <= 4, low-batch long context up to 32).  num_sms <= 0 means "the
- * current device's SM count".
+ * the S in 1..cap that minimises waves x (tiles per split + 4) + (S > 1 ? 2 : 0), with
+ * 64-row tiles, waves = ceil(T x S x ceil(H / 64) / num_sms) (one CTA per token, split and
+ * group of 64 heads, one CTA per SM) and 4 and 2 the fixed cost of a work item and of the
+ * combine in tiles; every split keeps >= 1 tile (vLLM PR #52212 report, "实现拆解" item 2:
+ * an occupancy target, low-batch long context up to 32 splits; that selector's cap of 4
+ * for short work is not kept: here a work item's fixed cost outweighs the combine, so
+ * short steps gain from more splits).  num_sms <= 0 means "the current device's SM
+ * count".
  */
 SMD_API int smd_select_num_splits(const smd_dims *dims, int num_splits, int num_sms);
 
