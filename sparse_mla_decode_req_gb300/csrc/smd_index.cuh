@@ -1,5 +1,4 @@
-// The index conversion rule, shared by the conversion kernels and the attention kernel's
-// index warps (which apply it in place of a conversion kernel).
+// The index conversion rule of the conversion kernels (dense, compacting).
 //
 // vLLM PR #41217 report, "关键源码片段", _convert_req_index_to_global_index_kernel: for
 // column j of token t the block is index // P and the in-page offset index % P; the block
@@ -12,10 +11,9 @@
 // column k of token t is masked when k >= TopkLength[t] (SGLang PR #26208 report,
 // "关键源码片段", HAS_TOPK_LENGTH).
 //
-// The rule runs in two halves around its one dependent load (the block-table entry), so
-// that a caller can keep several entries' loads in flight: index_block() checks the
-// request-local index and finds the block-table entry to read, index_slot() checks the
-// page read from it.
+// The rule runs in two halves around its one dependent load (the block-table entry):
+// index_block() checks the request-local index and finds the block-table entry to read,
+// index_slot() checks the page read from it.
 #pragma once
 
 #include "smd_device.cuh"
