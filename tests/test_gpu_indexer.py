@@ -245,6 +245,24 @@ def test_topk_ties_at_the_cut_take_the_lowest_positions():
     assert _np(got)[0].tolist() == [4000] + list(range(100, 160))
 
 
+@pytest.mark.parametrize("T,L", [(80, 12000), (80, 45000), (3, 30000)])
+def test_topk_rows_of_nearly_equal_logits(T, L):
+    """Rows whose logits almost all share the top 12 bits of their key, so that the keys
+    under the chosen digit outnumber the single-CTA kernel's 8192 candidate slots (80
+    tokens: the last pass then scans the row again, from shared memory at 12 000 positions,
+    from global memory at 45 000), and the clustered kernel's slices fill their candidate
+    lists (3 tokens)."""
+    g = torch.Generator(device="cuda").manual_seed(T + L)
+    lg = 1.0 + torch.rand(T, L, generator=g, device="cuda") * 1e-3   # one exponent, top mantissa bits alike
+    lg[:, ::997] = 2.5                                                # a few clear winners
+    lg[0, 5:40] = 1.0005                                              # equal values near the cut
+    ctx = torch.tensor([L - 7 * t for t in range(T)], dtype=torch.int32, device="cuda")
+    for K in (100, 2048):
+        got = api.indexer_topk(lg, ctx, K)
+        torch.cuda.synchronize()
+        _check_topk(got, lg, _np(ctx), K)
+
+
 # ----------------------------------------------------------------- indexer -> decode
 def test_indexer_topk_drives_the_decode():
     """Logits and top-k of the indexer over a key cache, then the sparse decode over the
