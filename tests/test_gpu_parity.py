@@ -285,6 +285,25 @@ def test_decode_poisoned_rows_are_scrubbed(kinds):
     assert_lse_close(lse, rl, "poison")
 
 
+@pytest.mark.parametrize("ns", [1, -3])
+def test_page_relocation_is_bit_identical(ns):
+    """The cache's pages moved to other places with the block table rewritten to match:
+    the same rows are read in the same order, so out and lse are bit for bit the same."""
+    w = synth.small_workload(num_tokens=5, num_heads=64, topk=300, swa=40, ctx=1200, n_invalid=9, extra_pages=4)
+    inp = synth.make_inputs(w, seed=123, device="cuda")
+    perm = torch.randperm(inp.kv_cache.shape[0], generator=torch.Generator().manual_seed(5)).cuda()
+    moved = torch.empty_like(inp.kv_cache)
+    moved[perm] = inp.kv_cache
+    bt = inp.block_table
+    bt2 = torch.where(bt >= 0, perm[bt.clamp_min(0).long()].to(torch.int32), bt)
+    a_out, a_lse = _run(inp, num_splits=ns)
+    b_out, b_lse = api.sparse_mla_decode(inp.q, moved, bt2, inp.req_id, inp.topk_idx, inp.swa_idx, inp.sink,
+                                         inp.scale, num_splits=ns, block_size=w.block_size)
+    torch.cuda.synchronize()
+    assert torch.equal(a_out.view(torch.int16), b_out.view(torch.int16))
+    assert torch.equal(a_lse.view(torch.int32), b_lse.view(torch.int32))
+
+
 def test_duplicates_and_shared_pages_across_tokens():
     """Entries repeated within a token and tokens sharing a request both count as given."""
     w = synth.small_workload(num_tokens=4, num_heads=16, topk=70, swa=10, ctx=300, n_invalid=0)

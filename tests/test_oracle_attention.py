@@ -191,3 +191,24 @@ def test_invalid_entries_are_masked_and_window_merges():
                                    **{**args, "req_id": args["req_id"][t:t + 1]})
         assert np.allclose(out[t], o2[0], rtol=1e-13, atol=1e-15)
         assert np.allclose(lse[t], l2[0], rtol=1e-13)
+
+
+@pytest.mark.parametrize("P", [64, 3])
+def test_page_relocation_changes_nothing(P):
+    """Moving every page of the cache to another place and rewriting the block table to
+    match reads the same rows in the same order: out and lse are bit-identical."""
+    w = synth.small_workload(num_tokens=3, num_heads=8, topk=70, swa=12, ctx=260, block_size=P, n_invalid=4,
+                             extra_pages=3)
+    inp = synth.make_inputs(w, seed=29 + P)
+    cache = inp.kv_cache.numpy()
+    perm = np.random.default_rng(P).permutation(cache.shape[0])  # page i moves to perm[i]
+    moved = np.empty_like(cache)
+    moved[perm] = cache
+    bt = inp.block_table.numpy()
+    bt2 = np.where(bt >= 0, perm[np.clip(bt, 0, None)], bt).astype(np.int32)
+    args = dict(req_id=inp.req_id.numpy(), topk_idx=inp.topk_idx.numpy(), swa_idx=inp.swa_idx.numpy(),
+                sink=inp.sink.double().numpy(), scale=inp.scale, block_size=P)
+    q = inp.q.double().numpy()
+    o1, l1 = sparse_mla_decode(q, kv_cache=cache, block_table=bt, **args)
+    o2, l2 = sparse_mla_decode(q, kv_cache=moved, block_table=bt2, **args)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
