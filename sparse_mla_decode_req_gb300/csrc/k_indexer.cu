@@ -338,6 +338,9 @@ __device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, 
   }
 }
 
+// IN_SMEM: the row's keys are kept in shared memory (rows up to kTopkSmemKeys positions);
+// otherwise every pass reads the row from global memory again.
+template <bool IN_SMEM>
 __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTopkParams p) {
   extern __shared__ uint32_t dyn[];  // [candidates][the row's keys when it fits]
   __shared__ uint32_t hist[kTopkBins1];
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTo
   const float* row = p.logits + (int64_t)t * p.stride;
   int32_t* out = p.topk + (int64_t)t * p.K;
   const int tid = threadIdx.x;
-  const bool in_smem = p.L <= kTopkSmemKeys;  // the launch gives L keys of shared memory then
+  constexpr bool in_smem = IN_SMEM;  // the launch gives L keys of shared memory then
   auto key_at = [&](int i) -> uint32_t { return in_smem ? skey[i] : order_key(__ldg(row + i)); };
 
   for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist[i] = 0u;
@@ -680,13 +683,17 @@ cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
   // positions in shared memory, longer ones re-read from global memory on every pass)
   static thread_local bool done[64] = {};
   if (dev < 0 || dev >= 64 || !done[dev]) {
-    e = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(indexer_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (kTopkCand + kTopkSmemKeys) * 4);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(indexer_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkCand * 4);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
-  const int keys = p.L <= kTopkSmemKeys ? p.L : 0;
-  indexer_topk_kernel<<<(unsigned)p.T, kTopkThreads, (size_t)(kTopkCand + keys) * 4, s>>>(p);
+  if (p.L <= kTopkSmemKeys)
+    indexer_topk_kernel<true><<<(unsigned)p.T, kTopkThreads, (size_t)(kTopkCand + p.L) * 4, s>>>(p);
+  else
+    indexer_topk_kernel<false><<<(unsigned)p.T, kTopkThreads, (size_t)kTopkCand * 4, s>>>(p);
   return cudaGetLastError();
 }
 
