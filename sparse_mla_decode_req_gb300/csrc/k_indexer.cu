@@ -297,8 +297,10 @@ __device__ __forceinline__ void count_and_compact(Load4 load4, int m, uint32_t m
 // positions and lane l takes every 32nd of them from l (shared-memory reads free of bank
 // conflicts); a position's rank is its warp's offset (one block-wide scan of the warps'
 // counts per step) plus the warp ballots of the positions before it.  base_gt and base_eq
-// come back advanced by the counts of [0, m).  Every thread of the block calls it.
-template <class KeyAt>
+// come back advanced by the counts of [0, m).  ONE_TIE: at most one key of the whole row
+// equals tau (the usual case), so its position goes straight to out[n_gt] and the ties take
+// no ballots (base_eq then comes back unchanged).  Every thread of the block calls it.
+template <bool ONE_TIE, class KeyAt>
 __device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, int need_eq, int n_gt, int pos0,
                                              int32_t* out, int& base_gt, int& base_eq, int (*wsum)[2]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -314,9 +316,13 @@ __device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, 
       const int i = w0 + 32 * k + lane;
       const uint32_t key = i < m ? key_at(i) : 0u;
       bg[k] = __ballot_sync(0xffffffffu, key != 0u && key > tau);
-      be[k] = __ballot_sync(0xffffffffu, tau != 0u && key == tau);
       cg += __popc(bg[k]);
-      ce += __popc(be[k]);
+      if constexpr (ONE_TIE) {
+        if (tau != 0u && key == tau) out[n_gt] = pos0 + i;
+      } else {
+        be[k] = __ballot_sync(0xffffffffu, tau != 0u && key == tau);
+        ce += __popc(be[k]);
+      }
     }
     int og, oe, tg, te;
     block_scan2(lane == 0 ? cg : 0, lane == 0 ? ce : 0, og, oe, tg, te, wsum);
@@ -326,12 +332,14 @@ __device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, 
     for (int k = 0; k < kSteps; ++k) {
       const int i = w0 + 32 * k + lane;
       if ((bg[k] >> lane) & 1u) out[og + __popc(bg[k] & before)] = pos0 + i;
-      if ((be[k] >> lane) & 1u) {
-        const int r = oe + __popc(be[k] & before);
-        if (r < need_eq) out[n_gt + r] = pos0 + i;
-      }
       og += __popc(bg[k]);
-      oe += __popc(be[k]);
+      if constexpr (!ONE_TIE) {
+        if ((be[k] >> lane) & 1u) {
+          const int r = oe + __popc(be[k] & before);
+          if (r < need_eq) out[n_gt + r] = pos0 + i;
+        }
+        oe += __popc(be[k]);
+      }
     }
     base_gt += tg;
     base_eq += te;
@@ -400,6 +408,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTo
 
   uint32_t tau = 0u;      // key of the K-th largest logit (0: take every finite one)
   int need_eq = 0;        // positions equal to tau to take
+  int n_tie = 0;          // positions equal to tau in the row
   if (total > p.K) {
     uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
     uint32_t remaining = s_left;
@@ -442,12 +451,18 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTo
     (void)pick_digit(hist, 1024u, remaining, wsum, &s_digit, &s_left);
     tau = prefix | s_digit;
     need_eq = (int)s_left;
+    n_tie = (int)hist[s_digit];  // keys equal to tau: all 32 bits chosen
   }
   const int n_gt = total > p.K ? p.K - need_eq : total;  // positions strictly above tau (all finite if none)
   // ordered pass: positions above tau ascending into [0, n_gt), then the lowest positions
   // equal to tau into [n_gt, K)
   int base_gt = 0, base_eq = 0;
-  ordered_pass(key_at, n, tau, need_eq, n_gt, 0, out, base_gt, base_eq, wsum);
+  if (n_tie <= 1) {
+    ordered_pass<true>(key_at, n, tau, need_eq, n_gt, 0, out, base_gt, base_eq, wsum);
+    base_eq = n_tie;
+  } else {
+    ordered_pass<false>(key_at, n, tau, need_eq, n_gt, 0, out, base_gt, base_eq, wsum);
+  }
   const int written = n_gt + (need_eq < base_eq ? need_eq : base_eq);
   for (int i = written + tid; i < p.K; i += kTopkThreads) out[i] = -1;
 }
@@ -545,6 +560,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(I
 
   uint32_t tau = 0u;
   int need_eq = 0;
+  int n_tie = 0;  // positions of the row equal to tau
   if (total > p.K) {  // the same decision in every CTA of the cluster
     uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
     uint32_t remaining = s_left;
@@ -581,6 +597,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(I
       prefix |= s_digit << shift;
       mask |= 1023u << shift;
       remaining = s_left;
+      if (shift == 0) n_tie = (int)mhist[s_digit];  // all 32 bits chosen: the keys equal to tau
       __syncthreads();
     }
     tau = prefix;
@@ -607,7 +624,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(I
   cluster_sync();  // the counts are read; the CTAs may now leave once done with their own memory
   // ordered pass over the slice: positions above tau at [base_gt, ...), the lowest equal ones
   // at n_gt + [base_eq, ...) while below need_eq
-  ordered_pass([&](int i) { return skey[i]; }, m, tau, need_eq, n_gt, s0, out, base_gt, base_eq, wsum);
+  if (n_tie <= 1)
+    ordered_pass<true>([&](int i) { return skey[i]; }, m, tau, need_eq, n_gt, s0, out, base_gt, base_eq, wsum);
+  else
+    ordered_pass<false>([&](int i) { return skey[i]; }, m, tau, need_eq, n_gt, s0, out, base_gt, base_eq, wsum);
   if (rank == 0) {
     const int written = n_gt + (need_eq < n_eq ? need_eq : n_eq);
     for (int i = written + tid; i < p.K; i += kTopkThreads) out[i] = -1;
