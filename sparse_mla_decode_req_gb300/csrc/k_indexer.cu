@@ -167,11 +167,13 @@ constexpr int kTopkCand = 8192;                      // candidates kept after th
 constexpr int kTopkBins1 = 4096;                     // first pass: the keys' top 12 bits
 
 // Order-preserving key of a logit: larger logit, larger key; -inf and NaN map to 0 and are
-// never selected; -0 is read as +0.
+// never selected; -0 is read as +0 (adding +0 turns it into +0).  A negative value's bits
+// all flip, a positive one's sign bit sets.  Every finite key is at least 2^23, so the top
+// 12 bits of key 0 (bin 0 of the first histogram) hold no finite logit.
 __device__ __forceinline__ uint32_t order_key(float x) {
-  if (!(x > -INFINITY)) return 0u;
-  const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(x + 0.0f);
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return x > -INFINITY ? k : 0u;
 }
 
 // Block-wide exclusive prefix sums of two per-thread counts (thread order) and their totals.
@@ -389,9 +391,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTo
       const int i0 = b0 + (u * kTopkThreads + tid) * 4;
       uint32_t kk[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 4; ++k) {  // past the row: -inf, key 0, not counted
         kk[k] = order_key(v[u][k]);
-        count_digit(kk[k], i0 + k < n, 0u, 0u, 20, kTopkBins1, hist);
+        if (kk[k] != 0u) atomicAdd(&hist[kk[k] >> 20], 1u);
       }
       if (in_smem) {  // one 16-byte store where all four are in the row
         if (i0 + 4 <= n) *reinterpret_cast<uint4*>(skey + i0) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
@@ -541,9 +543,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(I
       const int i0 = b0 + (u * kTopkThreads + tid) * 4;
       uint32_t kk[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 4; ++k) {  // past the slice: -inf, key 0, not counted
         kk[k] = order_key(v[u][k]);
-        count_digit(kk[k], i0 + k < m, 0u, 0u, 20, kTopkBins1, hist);
+        if (kk[k] != 0u) atomicAdd(&hist[kk[k] >> 20], 1u);
       }
       if (i0 + 4 <= m) *reinterpret_cast<uint4*>(skey + i0) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
       else
