@@ -217,7 +217,8 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& pa, int& pb, int&
 // mid-batch indexer shape).
 __device__ __forceinline__ void count_digit(uint32_t k, bool in, uint32_t mask, uint32_t prefix, int shift,
                                             uint32_t bins, uint32_t* hist) {
-  if (in && k != 0u && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1u)], 1u);
+  // prefix holds a finite key's top digit (>= 8), so key 0 never matches
+  if (in && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1u)], 1u);
 }
 
 // The digit holding the remaining-th largest counted key, scanning `bins` bins from the top,
@@ -266,7 +267,7 @@ __device__ __forceinline__ void count_and_compact(Load4 load4, int m, uint32_t m
     uint32_t hit = 0u;  // bit j: key j is under the prefix
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      if (k[j] != 0u && (k[j] & mask) == prefix) {
+      if ((k[j] & mask) == prefix) {  // a finite digit is >= 8, so key 0 never matches
         hit |= 1u << j;
         atomicAdd(&hist[(k[j] >> 10) & 1023u], 1u);
       }
@@ -317,7 +318,7 @@ __device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, 
     for (int k = 0; k < kSteps; ++k) {
       const int i = w0 + 32 * k + lane;
       const uint32_t key = i < m ? key_at(i) : 0u;
-      bg[k] = __ballot_sync(0xffffffffu, key != 0u && key > tau);
+      bg[k] = __ballot_sync(0xffffffffu, key > tau);  // key 0 (not finite) is never above tau
       cg += __popc(bg[k]);
       if constexpr (ONE_TIE) {
         if (tau != 0u && key == tau) out[n_gt] = pos0 + i;
