@@ -263,6 +263,29 @@ def test_topk_rows_of_nearly_equal_logits(T, L):
         _check_topk(got, lg, _np(ctx), K)
 
 
+def test_topk_ties_at_the_cut_single_cta_kernel():
+    """Many tokens (one CTA each): rows whose K-th largest value is shared by a run of
+    positions take the lowest of them, rows where it is unique take it alone, and the two
+    ordered-pass paths agree with the rule."""
+    T, L, K = 80, 3000, 61
+    g = torch.Generator(device="cuda").manual_seed(7)
+    lg = torch.randn(T, L, generator=g, device="cuda") - 10.0   # all below the planted values
+    for t in range(0, T, 2):                                      # even rows: 100 ties at the cut
+        lg[t, 100 + t:200 + t] = 3.0
+        lg[t, 2900] = 5.0
+    for t in range(1, T, 2):                                      # odd rows: distinct planted values
+        lg[t, 100:161] = torch.linspace(3.0, 4.0, 61, device="cuda")
+    ctx = torch.full((T,), L, dtype=torch.int32, device="cuda")
+    got = _np(api.indexer_topk(lg, ctx, K))
+    torch.cuda.synchronize()
+    for t in range(0, T, 2):
+        assert got[t].tolist() == [2900] + list(range(100 + t, 160 + t)), t
+    for t in range(1, T, 2):
+        assert sorted(got[t].tolist()) == list(range(100, 161)), t
+        assert got[t][-1] == 100 and np.all(np.diff(got[t][:-1]) > 0), t   # the K-th largest last
+    _check_topk(torch.from_numpy(got), lg, _np(ctx), K)
+
+
 # ----------------------------------------------------------------- indexer -> decode
 def test_indexer_topk_drives_the_decode():
     """Logits and top-k of the indexer over a key cache, then the sparse decode over the
