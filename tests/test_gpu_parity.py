@@ -218,6 +218,19 @@ def test_decode_small_shapes(H, N, P):
         assert_lse_close(lse, rl, f"H{H} N{N} P{P} splits {ns}")
 
 
+@pytest.mark.parametrize("splits", [-32, 0])
+def test_decode_long_index_lists(splits):
+    """65 573 entries per token (60 000 top-k + 5 573 window, 1 025 tiles, the last ragged),
+    1 000 of them -1, over contexts of 70 000 positions: 32 forced splits of 33 tiles, and
+    the selector's own choice."""
+    w = synth.small_workload(num_tokens=2, num_heads=16, topk=60000, swa=5573, ctx=70000, n_invalid=1000)
+    inp = synth.make_inputs(w, seed=4242, device="cuda")
+    out, lse = _run(inp, num_splits=splits)
+    ro, rl = oracle_decode(inp)
+    assert_out_close(out, ro, f"long lists splits {splits}")
+    assert_lse_close(lse, rl, f"long lists splits {splits}")
+
+
 @pytest.mark.parametrize("H", [40, 100, 127])
 def test_decode_partial_head_warps(H):
     """Head counts that leave a later softmax warp partly filled (its padding heads get no
