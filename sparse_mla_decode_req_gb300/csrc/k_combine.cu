@@ -35,6 +35,18 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
   constexpr float kLn2 = 0.6931471805599453f;
 
   const float ninf = -INFINITY;
+  // This lane's dims: 4 kNv consecutive ones from d0.  The first kPre splits' rows are
+  // loaded before the lse reduction, so that their round trip overlaps the lse one.
+  const int d0 = part * kDimsPerWarp + lane * 4 * kNv;
+  auto row_of = [&](int s) {
+    return reinterpret_cast<const float4*>(p.o_part + (((int64_t)t * p.S + s) * p.H + h) * kLatent + d0);
+  };
+  constexpr int kPre = 8 / kNv;  // splits preloaded (8 float4 per lane)
+  float4 pre[kPre][kNv];
+#pragma unroll
+  for (int s = 0; s < kPre; ++s)
+#pragma unroll
+    for (int i = 0; i < kNv; ++i) pre[s][i] = s < p.S ? __ldg(row_of(s) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   const float l_mine = lane < p.S ? __ldg(p.lse_part + ((int64_t)t * p.S + lane) * p.H + h) : ninf;
   const float sink = p.sink != nullptr ? __ldg(p.sink + h) : ninf;
   float M = l_mine;
@@ -42,8 +54,6 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   M = fmaxf(M, sink);
 
-  // This lane's dims: 4 kNv consecutive ones from d0.
-  const int d0 = part * kDimsPerWarp + lane * 4 * kNv;
   uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + (pair * kLatent + d0) * 2);
   const bool writes_lse = p.lse != nullptr && part == 0 && lane == 0;
   if (M == ninf) {  // no entries and no sink
@@ -64,10 +74,23 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(CombineParams p) {
   for (int i = 0; i < kNv; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   // Loads are unconditional (a batch of them in flight per unrolled group); a split of
   // weight 0 (lse -inf: no valid entries) contributes an exact 0 whatever its row holds.
+#pragma unroll
+  for (int s = 0; s < kPre; ++s) {
+    const float w = __shfl_sync(0xffffffffu, w_mine, s);  // 0 past S
+#pragma unroll
+    for (int i = 0; i < kNv; ++i) {
+      float4 v = pre[s][i];
+      if (w == 0.f) v = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[i].x = fmaf(w, v.x, acc[i].x);
+      acc[i].y = fmaf(w, v.y, acc[i].y);
+      acc[i].z = fmaf(w, v.z, acc[i].z);
+      acc[i].w = fmaf(w, v.w, acc[i].w);
+    }
+  }
 #pragma unroll(kNv == 4 ? 2 : kNv == 2 ? 4 : 8)
-  for (int s = 0; s < p.S; ++s) {
+  for (int s = kPre; s < p.S; ++s) {
     const float w = __shfl_sync(0xffffffffu, w_mine, s);
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + (((int64_t)t * p.S + s) * p.H + h) * kLatent + d0);
+    const float4* src = row_of(s);
 #pragma unroll
     for (int i = 0; i < kNv; ++i) {
       float4 v = __ldg(src + i);
