@@ -24,6 +24,8 @@
 //     The histograms are shared-memory atomics.
 #include <cuda.h>
 
+#include <utility>
+
 #include "smd_device.cuh"
 #include "smd_internal.h"
 
@@ -60,6 +62,7 @@ __device__ __forceinline__ GatherSrc gather_src(const IndexerGatherParams& p, in
 
 // Any layout and head_dim (a multiple of 4): one warp per token, 4-byte words.
 __global__ void __launch_bounds__(kGatherThreads) indexer_gather_kernel(IndexerGatherParams p) {
+  grid_dep_wait();  // launched as a programmatic dependent of the previous kernel
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (kGatherThreads / 32);
   for (int64_t tid = (int64_t)blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); tid < p.n; tid += warps) {
@@ -81,6 +84,7 @@ __global__ void __launch_bounds__(kGatherThreads) indexer_gather_kernel(IndexerG
 // head_dim / 16 lanes per token, one 16-byte load and store each, two tokens per group in
 // flight.
 __global__ void __launch_bounds__(kGatherThreads) indexer_gather16_kernel(IndexerGatherParams p) {
+  grid_dep_wait();
   const int lanes = p.D >> 4;                 // lanes per token
   const int groups = 32 / lanes;              // tokens per warp at a time
   const int lane = threadIdx.x & 31;
@@ -123,6 +127,7 @@ __global__ void __launch_bounds__(kGatherThreads) indexer_gather16_kernel(Indexe
 template <int PIECES>
 __global__ void __launch_bounds__(kGatherThreads, 4) indexer_gather_warp_kernel(IndexerGatherParams p) {
   static_assert(PIECES >= 1 && PIECES <= 32 && (PIECES & (PIECES - 1)) == 0, "a power of two up to 32");
+  grid_dep_wait();
   constexpr int kRound = PIECES < 8 ? PIECES : 8;  // pieces per lane in flight
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (kGatherThreads / 32);
@@ -353,6 +358,7 @@ __device__ __forceinline__ void ordered_pass(KeyAt key_at, int m, uint32_t tau, 
 // otherwise every pass reads the row from global memory again.
 template <bool IN_SMEM>
 __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_kernel(IndexerTopkParams p) {
+  grid_dep_wait();  // the logits kernel before it, launched as its programmatic dependent
   extern __shared__ uint32_t dyn[];  // [candidates][the row's keys when it fits]
   __shared__ uint32_t hist[kTopkBins1];
   __shared__ int wsum[kTopkWarps][2];
@@ -478,6 +484,7 @@ constexpr int kTkCluster = 4;
 constexpr int kTkSliceMax = 16 * 1024;   // keys per CTA
 
 __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(IndexerTopkParams p) {
+  grid_dep_wait();
   extern __shared__ uint32_t dyn[];        // [slice keys][candidates], kTkSliceMax each at most
   __shared__ uint32_t hist[kTopkBins1];    // this CTA's counts
   __shared__ uint32_t mhist[kTopkBins1];   // the cluster's counts
@@ -637,6 +644,25 @@ __global__ void __launch_bounds__(kTopkThreads, 2) indexer_topk_cluster_kernel(I
   }
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream: the grid may be
+// scheduled while that kernel finishes and waits for it (grid_dep_wait) before its first
+// global access.
+template <typename... Args, typename... Act>
+cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
+
 }  // namespace
 
 cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s) {
@@ -649,23 +675,19 @@ cudaError_t launch_indexer_gather(const IndexerGatherParams& p, cudaStream_t s) 
     int64_t blocks = (p.n + (kGatherThreads / 32) * 32 - 1) / ((kGatherThreads / 32) * 32);
     if (blocks > 65535 * 16) blocks = 65535 * 16;
     switch (pieces) {
-      case 1: indexer_gather_warp_kernel<1><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
-      case 2: indexer_gather_warp_kernel<2><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
-      case 4: indexer_gather_warp_kernel<4><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
-      case 8: indexer_gather_warp_kernel<8><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
-      case 16: indexer_gather_warp_kernel<16><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
-      default: indexer_gather_warp_kernel<32><<<(unsigned)blocks, kGatherThreads, 0, s>>>(p); break;
+      case 1: return launch_dependent(indexer_gather_warp_kernel<1>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
+      case 2: return launch_dependent(indexer_gather_warp_kernel<2>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
+      case 4: return launch_dependent(indexer_gather_warp_kernel<4>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
+      case 8: return launch_dependent(indexer_gather_warp_kernel<8>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
+      case 16: return launch_dependent(indexer_gather_warp_kernel<16>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
+      default: return launch_dependent(indexer_gather_warp_kernel<32>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
     }
-    return cudaGetLastError();
   }
   const int64_t per = (kGatherThreads / 32) * (fast ? 32 / (p.D / 16) * 2 : 1);  // tokens per CTA per step
   int64_t blocks = (p.n + per - 1) / per;
   if (blocks > 65535 * 16) blocks = 65535 * 16;
-  if (fast)
-    indexer_gather16_kernel<<<(unsigned)blocks, kGatherThreads, 0, s>>>(p);
-  else
-    indexer_gather_kernel<<<(unsigned)blocks, kGatherThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  if (fast) return launch_dependent(indexer_gather16_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
+  return launch_dependent(indexer_gather_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, p);
 }
 
 cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
@@ -693,13 +715,15 @@ cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
     cfg.blockDim = dim3(kTopkThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)2 * slice * 4;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kTkCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // a dependent of the logits kernel
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, indexer_topk_cluster_kernel, q);
   }
   // many tokens, or rows too long for the clusters: one CTA per token (rows up to 40 K
@@ -714,10 +738,10 @@ cudaError_t launch_indexer_topk(const IndexerTopkParams& p, cudaStream_t s) {
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
   if (p.L <= kTopkSmemKeys)
-    indexer_topk_kernel<true><<<(unsigned)p.T, kTopkThreads, (size_t)(kTopkCand + p.L) * 4, s>>>(p);
-  else
-    indexer_topk_kernel<false><<<(unsigned)p.T, kTopkThreads, (size_t)kTopkCand * 4, s>>>(p);
-  return cudaGetLastError();
+    return launch_dependent(indexer_topk_kernel<true>, dim3((unsigned)p.T), dim3(kTopkThreads),
+                            (size_t)(kTopkCand + p.L) * 4, s, p);
+  return launch_dependent(indexer_topk_kernel<false>, dim3((unsigned)p.T), dim3(kTopkThreads), (size_t)kTopkCand * 4,
+                          s, p);
 }
 
 }  // namespace smd

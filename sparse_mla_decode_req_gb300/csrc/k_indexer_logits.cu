@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kLgThreads) indexer_logits_kernel(const __grid
   const int tpc = kp.tiles_per_cta;
   const int tile0 = blockIdx.x * tpc;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_wait();  // launched as a programmatic dependent of the previous kernel
   float* const out = p.logits + (int64_t)t * p.L;
   const int ctx = min(__ldg(p.ctx_lens + t), p.L);
   const int ntiles = min(tpc, (ctx + kLgRows - 1) / kLgRows - tile0);  // tiles with positions < ctx
@@ -292,8 +293,17 @@ cudaError_t launch_logits_h(const LogitsKernelParams& kp, cudaStream_t s) {
   LogitsKernelParams k2 = kp;
   k2.tiles_per_cta = (int)tpc;
   const dim3 grid((unsigned)((tiles_row + tpc - 1) / tpc), (unsigned)kp.p.T);
-  indexer_logits_kernel<H><<<grid, kLgThreads, smem, s>>>(k2);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kLgThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];  // a programmatic dependent of the previous kernel (grid_dep_wait above)
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, indexer_logits_kernel<H>, k2);
 }
 
 }  // namespace
