@@ -8,6 +8,8 @@
   logits (both sides decide in float32) must give the same position sets;
 * the indexer's top-k positions fed to the sparse decode.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -137,16 +139,47 @@ def test_logits_masks_bad_pages_requests_and_short_rows():
     _check_logits(got, inp, L)
 
 
-def test_logits_full_size_sampled():
-    """The mid-batch indexer shape (32 requests, context U[4096, 32768], 64 heads of 128)
-    in the launch the benchmark times; six sampled tokens against the oracle."""
-    w = si.INDEXER_WORKLOADS[0]
+@pytest.mark.parametrize("which,toks", [(0, [0, 1, "argmax", "argmin", 17, 31]), (1, [0, 1, 128, 255])])
+def test_logits_full_size_sampled(which, toks):
+    """The mid-batch indexer shape (32 requests, context U[4096, 32768]: CTAs wholly past
+    a row's context write -inf only) and the large-batch one (256 requests of 8192), 64
+    heads of 128, in the launch the benchmark times: every entry written (the output
+    starts as NaN), sampled tokens against the oracle."""
+    w = si.INDEXER_WORKLOADS[which]
     inp = si.make_indexer_inputs(w, device="cuda")
     L = inp.max_len
-    got = api.indexer_mqa_logits(inp.q, inp.weights, inp.cache, inp.block_table, inp.req_id, inp.ctx_lens, L)
+    out = torch.full((w.num_tokens, L), float("nan"), dtype=torch.float32, device="cuda")
+    got = api.indexer_mqa_logits(inp.q, inp.weights, inp.cache, inp.block_table, inp.req_id, inp.ctx_lens, L,
+                                 logits=out)
     torch.cuda.synchronize()
-    toks = [0, 1, int(np.argmax(inp.ctx)), int(np.argmin(inp.ctx)), 17, 31]
-    _check_logits(got, inp, L, toks)
+    assert not bool(torch.isnan(got).any())
+    pick = {"argmax": int(np.argmax(inp.ctx)), "argmin": int(np.argmin(inp.ctx))}
+    _check_logits(got, inp, L, [pick.get(t, t) for t in toks])
+
+
+def _inputs_with_contexts(ctx, seed, H=64, P=64):
+    """Indexer inputs whose tokens have the given contexts (pages for the longest one each)."""
+    top = max(max(ctx), 1)
+    w = si.small_indexer_workload(num_tokens=len(ctx), ctx_lo=top, ctx_hi=top, num_heads=H, block_size=P,
+                                  extra_pages=2)
+    inp = si.make_indexer_inputs(w, seed=seed, device="cuda")
+    return dataclasses.replace(inp, ctx_lens=torch.tensor(ctx, dtype=torch.int32, device="cuda"), ctx=list(ctx))
+
+
+@pytest.mark.parametrize("ctx,L", [([0, 0, 5000, 0], 5000), ([32768], 32768), ([70000, 0, 5], 70000),
+                                   ([12000] * 80, 12000), ([1] * 900, 1), ([0] * 40, 300),
+                                   ([3000, 128, 129, 127, 1, 0, 2999, 640], 3001)])
+def test_logits_ragged_rows_write_every_entry(ctx, L):
+    """Ragged rows (empty ones, one position, a partial last tile, rows of 70 000, 900
+    tokens): every entry written (the output starts as NaN), sampled rows against the
+    oracle."""
+    inp = _inputs_with_contexts(ctx, seed=len(ctx) + L % 97)
+    out = torch.full((len(ctx), L), float("nan"), dtype=torch.float32, device="cuda")
+    got = api.indexer_mqa_logits(inp.q, inp.weights, inp.cache, inp.block_table, inp.req_id, inp.ctx_lens, L,
+                                 logits=out)
+    torch.cuda.synchronize()
+    assert not bool(torch.isnan(got).any())
+    _check_logits(got, inp, L, sorted({0, len(ctx) // 2, len(ctx) - 1}))
 
 
 def test_gather_full_size_prefix():
