@@ -231,12 +231,12 @@ def _check_topk(got, logits_gpu, ctx, K):
             assert np.all(np.diff(a) > 0)
 
 
-@pytest.mark.parametrize("T,L,K", [(3, 5000, 512), (2, 300, 400), (4, 70000, 2048), (1, 1, 1), (80, 3000, 256),
-                                   (96, 45000, 2048)])
+@pytest.mark.parametrize("T,L,K", [(3, 5000, 512), (2, 300, 400), (4, 70000, 2048), (2, 120000, 2048), (1, 1, 1),
+                                   (50, 20000, 1024), (50, 60000, 2048), (80, 3000, 256), (96, 45000, 2048)])
 def test_topk_on_synthetic_logits(T, L, K):
-    """Few tokens take the clustered kernel (four CTAs per token), many tokens or rows past
-    64 K positions one CTA per token (keys in shared memory up to 40 K positions, else read
-    from global memory on every pass)."""
+    """Few tokens take the clustered kernel (four CTAs per token; on 152 SMs up to 76
+    tokens), many tokens or rows past 64 K positions one CTA per token (keys in shared
+    memory up to 40 K positions, else read from global memory on every pass)."""
     g = torch.Generator(device="cuda").manual_seed(T * L + K)
     lg = torch.randn(T, L, generator=g, device="cuda")
     if L > 100:
@@ -278,13 +278,13 @@ def test_topk_ties_at_the_cut_take_the_lowest_positions():
     assert _np(got)[0].tolist() == [4000] + list(range(100, 160))
 
 
-@pytest.mark.parametrize("T,L", [(80, 12000), (80, 45000), (3, 30000)])
+@pytest.mark.parametrize("T,L", [(80, 12000), (80, 45000), (3, 30000), (50, 30000)])
 def test_topk_rows_of_nearly_equal_logits(T, L):
     """Rows whose logits almost all share the top 12 bits of their key, so that the keys
     under the chosen digit outnumber the single-CTA kernel's 8192 candidate slots (80
     tokens: the last pass then scans the row again, from shared memory at 12 000 positions,
-    from global memory at 45 000), and the clustered kernel's slices fill their candidate
-    lists (3 tokens)."""
+    from global memory at 45 000), and the clustered kernels' slices fill their candidate
+    lists (3 and 50 tokens)."""
     g = torch.Generator(device="cuda").manual_seed(T + L)
     lg = 1.0 + torch.rand(T, L, generator=g, device="cuda") * 1e-3   # one exponent, top mantissa bits alike
     lg[:, ::997] = 2.5                                                # a few clear winners
